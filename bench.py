@@ -1,0 +1,392 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step = one attn_fwd call over the whole workload (default: the
+long-context causal workload B=1, h=32, L=32768, d=128, whose Q/K/V (805 MB)
+are larger than L2, so no L2 flush is needed between steps).  Prints one JSON
+line.  Under torchrun (N > 1) every rank runs an independent replica of the
+workload on its own GPU (weak scaling; attention has no cross-sequence
+exchange), the timed region is bracketed by barriers, and the max time over
+ranks is reported.
+
+--impl reference times the fp64 CPU oracle (the reference implementation of
+this method) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sdpa_workloads import (BENCH_WORKLOAD, MASK_CAUSAL, MASK_PADDING, WORKLOADS,  # noqa: E402
+                            attn_flops, make_workload_inputs)
+
+METRIC = "attention fwd TFLOP/s on 1 GB300 and % of roofline (tensor/exp/HBM bound)"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+MUFU_EXP_PER_S = 10.7e12  # nominal ex2 rate of the part (not measured)
+KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "ptx.cuh"]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "transformer_scaled_dot_sdpa_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    ent = d.get(workload)
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def algorithmic_counts(w, kv_lens):
+    """FLOPs, exponentials and HBM bytes of one pass (definitions in the design doc)."""
+    flops = attn_flops(w.B, w.H, w.Lq, w.Lk, w.d_k, w.mask_kind, kv_lens)
+    exps = flops / (4.0 * w.d_k)            # one exp per unmasked score
+    qkv_bytes = 2.0 * w.B * w.H * (w.Lq * w.d_k + w.Lk * (w.d_k + w.d_v))
+    out_bytes = 2.0 * w.B * w.H * w.Lq * w.d_v + 4.0 * w.B * w.H * w.Lq
+    return flops, exps, qkv_bytes + out_bytes
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        load = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle on a bounded sample of the workload
+# ---------------------------------------------------------------------------
+def oracle_sample_rows(w, rows_per_head):
+    """Stratified query rows of every head (flat ids (b*H + h)*Lq + i)."""
+    stride = max(1, w.Lq // rows_per_head)
+    per = np.arange(stride // 2, w.Lq, stride, dtype=np.int64)[:rows_per_head]
+    return np.concatenate([bh * w.Lq + per for bh in range(w.B * w.H)])
+
+
+def oracle_row_flops(w, rows, kv_lens):
+    tot = 0.0
+    for r in rows:
+        i = int(r % w.Lq)
+        b = int(r // (w.H * w.Lq))
+        n = w.Lk
+        if w.mask_kind & MASK_CAUSAL:
+            n = min(n, i + 1)
+        if w.mask_kind & MASK_PADDING:
+            n = 0 if i >= kv_lens[b] else min(n, int(kv_lens[b]))
+        tot += 4.0 * n * w.d_k
+    return tot
+
+
+def run_oracle_sample(w, inp, rows_per_head):
+    import oracle
+    rows = oracle_sample_rows(w, rows_per_head)
+    t0 = time.perf_counter()
+    oracle.attention(inp["q"], inp["k"], inp["v"], mask_kind=w.mask_kind,
+                     kv_lens=inp["kv_lens"], scale=w.scale, rows=rows)
+    dt = time.perf_counter() - t0
+    fl = oracle_row_flops(w, rows, inp["kv_lens"])
+    return fl, dt, len(rows), oracle.default_threads()
+
+
+def reference_arm(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    inp = make_workload_inputs(w)
+    rows_per_head = max(1, args.ref_rows // (w.B * w.H))
+    times, flops = [], 0.0
+    cores = None
+    for i in range(args.warmup + args.steps):
+        fl, dt, n, cores = run_oracle_sample(w, inp, rows_per_head)
+        if i >= args.warmup:
+            times.append(dt)
+            flops = fl
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms * 1e-3) / 1e12
+    sample = "%d query rows per step (%d of each of the %d heads, stratified), fp64" % (
+        rows_per_head * w.B * w.H, rows_per_head, w.B * w.H)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, world):
+    mask = {0: "none", 1: "causal", 2: "padding", 3: "causal+padding"}[w.mask_kind]
+    return {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d_k,
+            "mask": mask, "parallelism": "replicas x%d" % world,
+            "l2": "inputs larger than L2 (Q/K/V %.0f MB), no flush" %
+                  (2.0 * w.B * w.H * (w.Lq + 2 * w.Lk) * w.d_k / 1e6)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def ours_arm(args, w):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import transformer_scaled_dot_sdpa_gb300 as g
+
+    # replicas draw distinct data (independent problems)
+    w_rank = w if rank == 0 else type(w)(**{**w.__dict__, "seed": w.seed + 7919 * rank})
+    inp = make_workload_inputs(w_rank)
+    kv_lens = inp["kv_lens"]
+
+    def pinned(bits):
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory()
+
+    hq, hk, hv = pinned(inp["q"]), pinned(inp["k"]), pinned(inp["v"])
+    q = hq.to(dev)
+    k = hk.to(dev)
+    v = hv.to(dev)
+    kvt = torch.from_numpy(kv_lens).to(dev) if kv_lens is not None else None
+    O = torch.empty((w.B, w.H, w.Lq, w.d_v), dtype=torch.bfloat16, device=dev)
+    LSE = torch.empty((w.B, w.H, w.Lq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        g.attn_fwd(q, k, v, mask_kind=w.mask_kind, kv_lens=kvt, scale=w.scale, out=O, lse=LSE,
+                   stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    g.check_device_status(stream)
+
+    clocks = ClockSampler(dev.index if world == 1 else local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    g.check_device_status(stream)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms_max = max_over_ranks(ms, world)
+
+    # end to end through the public API with host buffers: pinned H2D of the
+    # inputs, the attention call, D2H of O and LSE, every step
+    hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    hL = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        hO.copy_(O, non_blocking=True)
+        hL.copy_(LSE, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    g.check_device_status(stream)
+
+    flops, exps, hbm_bytes = algorithmic_counts(w, kv_lens)
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    tensor_peak = peaks["bf16_tflops"] * 1e12
+    hbm_peak = peaks["hbm_gbs"] * 1e9
+    t_tensor = flops / tensor_peak
+    t_exp = exps / MUFU_EXP_PER_S
+    t_hbm = hbm_bytes / hbm_peak
+    bound = max((t_tensor, "tensor"), (t_hbm, "hbm"), (t_exp, "exp"))[1]
+    achieved_tflops = flops / (ms * 1e-3) / 1e12   # this rank's kernel
+    roofline = {
+        "bound": "tensor" if bound in ("tensor", "exp") else "hbm",
+        "achieved": achieved_tflops if bound != "hbm" else hbm_bytes / (ms * 1e-3) / 1e9,
+        "peak": peaks["bf16_tflops"] if bound != "hbm" else peaks["hbm_gbs"],
+        "unit": "TFLOP/s" if bound != "hbm" else "GB/s",
+        "traffic": profiled_traffic(w.name),
+        "peak_source": "%s (bf16 dense burst)" % peak_src if bound != "hbm" else peak_src,
+        "kernel": "attn_fwd_kernel<%d>" % w.d_k,
+        "roofline_time_ms": 1e3 * max(t_tensor, t_exp, t_hbm),
+        "frac_of_roofline_time": 1e3 * max(t_tensor, t_exp, t_hbm) / ms,
+        "exp_bound_fraction": t_exp / max(t_tensor, t_hbm),
+    }
+    roofline["frac"] = roofline["achieved"] / roofline["peak"]
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fl, dt, n, cores = run_oracle_sample(w, inp, max(1, args.cpu_rows // (w.B * w.H)))
+        cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "%d query rows (stratified over all %d heads), %.3g FLOP in %.1f s"
+                         % (n, w.B * w.H, fl, dt)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, world),
+        "e2e": {"value": e2e_value, "unit": UNIT,
+                "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
+                "d2h_bytes_per_step": int(hO.numel() * 2 + hL.numel() * 4),
+                "steps": e2e_steps, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=sorted(
+        n for n, w in WORKLOADS.items() if w.kind == "attn"))
+    ap.add_argument("--cpu-rows", type=int, default=65536,
+                    help="query rows the CPU oracle baseline computes")
+    ap.add_argument("--ref-rows", type=int, default=512,
+                    help="query rows per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, w)
+    return ours_arm(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,153 @@
+/*
+ * gb300attn.h -- C ABI of the GB300 (sm_103a) multi-head scaled dot-product
+ * attention library (libgb300attn.so).
+ *
+ * The operation, as the tutorial pages define it:
+ *
+ *   Attention(Q, K, V) = softmax(Q K^T / sqrt(d_k) + M) V
+ *     "04. Self-Attention：Transformer 的核心计算", section 四 (scores,
+ *     scale, row softmax, weighted sum) and section 七 (the mask M is added
+ *     before the softmax: 0 where a key may be seen, -inf where it may not).
+ *   Causal mask: key j is hidden from query i when j > i ("attention-mechanism"
+ *     page, section "掩码：因果与 padding").  Padding mask: keys at or past
+ *     the sequence's valid length are hidden (same section).
+ *   Multi-head layer: Y = Concat(head_1..head_h) W_O with
+ *     head_i = Attention(X W_Q^i, X W_K^i, X W_V^i), the three projections
+ *     fused into one GEMM with W_QKV = [W_Q | W_K | W_V] ("Self-Attention 机制",
+ *     sections "五步计算" and "维度全程跟踪").
+ *
+ * Conventions for every entry point:
+ *   - All tensors are dense, row-major, in DEVICE memory, and owned by the
+ *     caller; the library keeps no pointer after a call returns.
+ *   - Element types: bf16 (bfloat16) for Q, K, V, O, X, weights and Y; float
+ *     for LSE; int32 for kv_lens.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous: errors found on the host are returned before anything
+ *     is launched; errors found on the device are reported later by
+ *     attn_check_device_status().
+ *   - The library allocates no device memory per call.  It keeps, per device
+ *     and for the life of the process, a 4-byte device status word (a file-
+ *     scope __device__ variable) and cached kernel attributes.
+ *   - Thread safety: calls may be made from several host threads; calls on
+ *     one stream execute in order.
+ */
+#ifndef GB300ATTN_H
+#define GB300ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* bad size, null pointer, kv_len out of range */
+  ATTN_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement  */
+  ATTN_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned            */
+  ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed            */
+  ATTN_ERR_TIMEOUT = 5       /* a device-side pipeline wait gave up          */
+} attn_status_t;
+
+/* mask_kind bit flags; ATTN_MASK_CAUSAL | ATTN_MASK_PADDING applies both */
+enum { ATTN_MASK_NONE = 0, ATTN_MASK_CAUSAL = 1, ATTN_MASK_PADDING = 2 };
+
+/*
+ * attn_fwd -- multi-head attention forward over [B, h, L, d] heads.
+ *
+ *   Q  bf16 [B, h, Lq, d_k]     K  bf16 [B, h, Lk, d_k]     V  bf16 [B, h, Lk, d_v]
+ *   O  bf16 [B, h, Lq, d_v]     (written)
+ *   LSE float [B, h, Lq]        (written when non-NULL) natural-log
+ *                               log-sum-exp of the row's scaled, masked scores
+ *   kv_lens int32 [B] device array, required iff mask_kind has the PADDING
+ *     bit: sequence b's valid length.  Keys j >= kv_lens[b] are masked; query
+ *     rows i >= kv_lens[b] are padding and get O = 0, LSE = -inf.
+ *   mask_kind: ATTN_MASK_* flags.  CAUSAL hides key j from query i when j > i
+ *     (top-left aligned when Lq != Lk).
+ *   scale: multiplier of Q K^T; scale <= 0 selects 1 / sqrt(d_k).
+ *   A row with no visible key (kv_lens[b] == 0, or Lk == 0) gets O = 0 and
+ *   LSE = -inf.  The attention matrix itself is never formed or returned.
+ *
+ * Supported: d_k == d_v in {64, 128}; B, h, Lq, Lk >= 0 with B*h*ceil(Lq/256)
+ * < 2^31 and Lq, Lk < 2^31.  Q, K, V, O must be 16-byte aligned, LSE 4-byte
+ * aligned.  Empty problems (B, h or Lq == 0) return ATTN_OK without a launch.
+ * A kv_lens entry outside [0, Lk] is clamped on the device and reported as
+ * ATTN_ERR_INVALID_ARG by attn_check_device_status().
+ */
+attn_status_t attn_fwd(const void* Q, const void* K, const void* V, int B, int h, int Lq, int Lk,
+                       int d_k, int d_v, int mask_kind, const int32_t* kv_lens, float scale,
+                       void* O, float* LSE, void* stream);
+
+/*
+ * mha_layer_workspace_bytes -- device workspace mha_layer_fwd needs for this
+ * shape: the fused projection QKV bf16 [B, L, 3, h, d_k] plus the concatenated
+ * heads bf16 [B, L, d_model].  Returns 0 for an unsupported shape.
+ */
+size_t mha_layer_workspace_bytes(int B, int L, int d_model, int h);
+
+/*
+ * mha_layer_fwd -- the five-step multi-head self-attention layer:
+ *   QKV = X W_QKV               (one GEMM; W_QKV columns are [Q | K | V], head
+ *                                i owning columns i*d_k .. i*d_k+d_k-1 of each)
+ *   O_i = Attention(Q_i, K_i, V_i) with the given mask, d_k = d_model / h
+ *   Y   = Concat(O_1 .. O_h) W_O
+ *
+ *   X bf16 [B, L, d_model];  W_QKV bf16 [d_model, 3*d_model];
+ *   W_O bf16 [d_model, d_model];  Y bf16 [B, L, d_model] (written).
+ *   The weights multiply from the right (X W, W stored [in, out]); there are
+ *   no biases.  kv_lens / mask_kind / scale as for attn_fwd.  Padded query
+ *   rows produce Y = 0.
+ *   workspace: device buffer of at least mha_layer_workspace_bytes(), 256-byte
+ *   aligned; it is scratch, overwritten by the call.
+ *
+ * Supported: d_model / h in {64, 128}, d_model a multiple of 128, B*L a
+ * multiple of 128; all pointers 16-byte aligned.
+ */
+attn_status_t mha_layer_fwd(const void* X, const void* W_QKV, const void* W_O, int B, int L,
+                            int d_model, int h, int mask_kind, const int32_t* kv_lens,
+                            float scale, void* Y, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * attn_gemm_bf16 -- C = A B with bf16 inputs, fp32 accumulation and bf16
+ * output: the projection step of the layer, exposed for direct use.
+ *   A bf16 [M, K], B bf16 [K, N], C bf16 [M, N], all row-major.
+ * Supported: M multiple of 128, N multiple of 256, K multiple of 64;
+ * pointers 16-byte aligned.
+ */
+attn_status_t attn_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K,
+                             void* stream);
+
+/*
+ * attn_check_device_status -- synchronize `stream`, then read and clear the
+ * current device's status word.  Returns ATTN_ERR_TIMEOUT if a kernel's
+ * bounded pipeline wait gave up since the last check, ATTN_ERR_INVALID_ARG if
+ * a kv_lens entry was out of range, ATTN_ERR_CUDA if the stream reports a
+ * CUDA error, else ATTN_OK.
+ */
+attn_status_t attn_check_device_status(void* stream);
+
+/* attn_status_string -- static, human-readable name of a status code. */
+const char* attn_status_string(attn_status_t status);
+
+/*
+ * attn_set_wait_limit_ns -- time limit of every device-side pipeline wait
+ * (default 2e9 ns).  After it, the kernel stops, records ATTN_ERR_TIMEOUT in
+ * the status word and returns instead of waiting forever.  0 restores the
+ * default.  Affects launches made after the call.
+ */
+void attn_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * attn_debug_skip_kv_load -- testing hook: the next attn_fwd launches skip
+ * the K-tile load with this running index in every CTA, so that a pipeline
+ * wait runs out and the timeout path is exercised (-1 disables; the default).
+ */
+void attn_debug_skip_kv_load(long long index);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300ATTN_H */

@@ -1,0 +1,107 @@
+"""The C ABI boundary, checked without a GPU: the library loads, exports every
+function include/gb300attn.h declares, and rejects bad arguments on the host
+before any CUDA call."""
+import ctypes
+import importlib.util
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gb300attn.h")
+
+
+def _build():
+    spec = importlib.util.spec_from_file_location(
+        "_gb300attn_build", os.path.join(ROOT, "transformer_scaled_dot_sdpa_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()
+
+
+@pytest.fixture(scope="module")
+def cdll():
+    path = _build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["attn_fwd", "mha_layer_fwd", "mha_layer_workspace_bytes", "attn_check_device_status",
+              "attn_status_string", "attn_gemm_bf16", "attn_set_wait_limit_ns",
+              "attn_debug_skip_kv_load"]:
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(cdll):
+    missing = [n for n in declared_functions() if not hasattr(cdll, n)]
+    assert not missing, missing
+
+
+def test_status_strings(cdll):
+    f = cdll.attn_status_string
+    f.restype = ctypes.c_char_p
+    f.argtypes = [ctypes.c_int]
+    assert f(0) == b"ATTN_OK"
+    assert f(5) == b"ATTN_ERR_TIMEOUT"
+    assert f(99) == b"ATTN_STATUS_UNKNOWN"
+
+
+def _attn(cdll):
+    f = cdll.attn_fwd
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    f.restype = i
+    f.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, ctypes.c_float, vp, vp, vp]
+    return f
+
+
+def test_host_validation_before_any_cuda_call(cdll):
+    f = _attn(cdll)
+    p = ctypes.c_void_p(0x1000)
+    INVALID, UNSUPPORTED, MISALIGNED = 1, 2, 3
+    # negative sizes, unknown mask bits, NaN scale
+    assert f(p, p, p, -1, 1, 8, 8, 64, 64, 0, None, 0.0, p, None, None) == INVALID
+    assert f(p, p, p, 1, 1, 8, 8, 64, 64, 4, None, 0.0, p, None, None) == INVALID
+    assert f(p, p, p, 1, 1, 8, 8, 64, 64, 0, None, float("nan"), p, None, None) == INVALID
+    # head dims this build does not implement
+    assert f(p, p, p, 1, 1, 8, 8, 96, 96, 0, None, 0.0, p, None, None) == UNSUPPORTED
+    assert f(p, p, p, 1, 1, 8, 8, 64, 128, 0, None, 0.0, p, None, None) == UNSUPPORTED
+    # padding without lengths, null output
+    assert f(p, p, p, 1, 1, 8, 8, 64, 64, 2, None, 0.0, p, None, None) == INVALID
+    assert f(p, p, p, 1, 1, 8, 8, 64, 64, 0, None, 0.0, None, None, None) == INVALID
+    # misaligned pointers (TMA needs 16-byte aligned bases)
+    bad = ctypes.c_void_p(0x1008)
+    assert f(bad, p, p, 1, 1, 8, 8, 64, 64, 0, None, 0.0, p, None, None) == MISALIGNED
+    assert f(p, p, p, 1, 1, 8, 8, 64, 64, 0, None, 0.0, bad, None, None) == MISALIGNED
+    # empty problems succeed without touching the device
+    assert f(None, None, None, 0, 4, 8, 8, 64, 64, 0, None, 0.0, None, None, None) == 0
+    assert f(None, None, None, 2, 4, 0, 8, 64, 64, 0, None, 0.0, None, None, None) == 0
+
+
+def test_layer_and_gemm_validation(cdll):
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    ws = cdll.mha_layer_workspace_bytes
+    ws.restype = sz
+    ws.argtypes = [i, i, i, i]
+    assert ws(8, 2048, 1024, 16) == 8 * 2048 * 3 * 1024 * 2 + 8 * 2048 * 1024 * 2
+    assert ws(1, 1, 100, 3) == 0
+    lay = cdll.mha_layer_fwd
+    lay.restype = i
+    lay.argtypes = [vp, vp, vp, i, i, i, i, i, vp, ctypes.c_float, vp, vp, sz, vp]
+    p = ctypes.c_void_p(0x1000)
+    assert lay(p, p, p, 1, 128, 1000, 10, 0, None, 0.0, p, p, 1 << 30, None) == 2  # d_k = 100
+    assert lay(p, p, p, 1, 100, 1024, 16, 0, None, 0.0, p, p, 1 << 30, None) == 2  # B*L % 128
+    assert lay(p, p, p, 1, 128, 1024, 16, 0, None, 0.0, p, p, 16, None) == 1      # workspace
+    g = cdll.attn_gemm_bf16
+    g.restype = i
+    g.argtypes = [vp, vp, vp, i, i, i, vp]
+    assert g(p, p, p, 100, 256, 64, None) == 2
+    assert g(p, p, p, -1, 256, 64, None) == 1

@@ -1,0 +1,82 @@
+"""GPU parity of the projection GEMM and of the five-step layer
+(QKV projection -> split heads -> attention -> concat -> W_O) against the
+fp64 oracle."""
+import numpy as np
+import pytest
+
+import oracle
+from sdpa_workloads import (MASK_CAUSAL, MASK_NONE, MASK_PADDING, WORKLOADS, bf16_to_f32,
+                            f64_to_bf16_bits, make_layer_inputs, make_workload_inputs,
+                            sample_rows)
+from tests.parity_util import O_MAX_ABS, O_MEAN_ABS, down, up
+
+pytestmark = pytest.mark.gpu
+
+
+def _gemm_case(M, N, K, seed):
+    rng = np.random.default_rng(seed)
+    a = f64_to_bf16_bits(rng.standard_normal((M, K)))
+    b = f64_to_bf16_bits(rng.standard_normal((K, N)) / np.sqrt(K))
+    return a, b
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 192), (384, 768, 1024),
+                                   (1024, 3072, 1024)])
+def test_gemm_matches_fp64_matmul(cuda_lib, M, N, K):
+    """C = A B: bf16 inputs, fp32 accumulation, one bf16 rounding of the
+    result.  The fp64 product of the same bf16 values (a library matmul) is
+    the reference; the bound is half a bf16 ulp (2^-8 relative) plus fp32
+    accumulation slack."""
+    a, b = _gemm_case(M, N, K, seed=M + N + K)
+    C = down(cuda_lib.gemm_bf16(up(a), up(b)))
+    cuda_lib.check_device_status()
+    ref = bf16_to_f32(a).astype(np.float64) @ bf16_to_f32(b).astype(np.float64)
+    err = np.abs(C - ref)
+    bound = 2.0 ** -8 * np.abs(ref) + 1e-5 * np.sqrt(K)
+    assert np.all(err <= bound), "max excess %.3g" % (err - bound).max()
+
+
+def _layer_run(g, inp, H, mask, kv=None):
+    import torch
+    kvt = torch.from_numpy(kv).cuda() if kv is not None else None
+    Y = g.mha_layer_fwd(up(inp["x"]), up(inp["w_qkv"]), up(inp["w_o"]), H, mask_kind=mask,
+                        kv_lens=kvt)
+    g.check_device_status()
+    return down(Y)
+
+
+def _compare(Y, Yr, what):
+    err = np.abs(Y - Yr)
+    assert np.all(np.isfinite(Y)), what
+    assert err.max() <= O_MAX_ABS, "%s: max abs err %.4g" % (what, err.max())
+    assert err.mean() <= O_MEAN_ABS, "%s: mean abs err %.4g" % (what, err.mean())
+
+
+@pytest.mark.parametrize("B,L,dm,H", [(1, 128, 256, 4), (2, 192, 512, 8), (1, 384, 512, 4),
+                                      (2, 320, 768, 12)])
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_PADDING,
+                                  MASK_CAUSAL | MASK_PADDING])
+def test_layer_small(cuda_lib, B, L, dm, H, mask):
+    inp = make_layer_inputs(B, L, dm, seed=B * L + dm + mask, w_std=1.0 / np.sqrt(dm))
+    kv = np.array([L, L // 3, 1, 0][:B], dtype=np.int32) if mask & MASK_PADDING else None
+    Y = _layer_run(cuda_lib, inp, H, mask, kv)
+    Yr = oracle.mha_layer(inp["x"], inp["w_qkv"], inp["w_o"], H, mask_kind=mask, kv_lens=kv)
+    _compare(Y, Yr, "layer B%d L%d dm%d H%d mask%d" % (B, L, dm, H, mask))
+    if kv is not None:
+        for b in range(B):
+            assert np.all(Y[b, kv[b]:] == 0.0)
+
+
+def test_layer_workload_sampled(cuda_lib):
+    """The full layer workload (B=8, L=2048, d_model=1024, 16 heads, causal)
+    in the benchmark's launch configuration; the oracle computes sampled rows
+    of two sequences."""
+    w = WORKLOADS["mha_layer_causal_b8_l2048_dm1024_h16"]
+    inp = make_workload_inputs(w)
+    Y = _layer_run(cuda_lib, inp, w.H, w.mask_kind)
+    assert np.all(np.isfinite(Y))
+    rows = sample_rows(w.L, 40, seed=w.seed)
+    flat = np.concatenate([0 * w.L + rows, 5 * w.L + rows])
+    Yr = oracle.mha_layer(inp["x"], inp["w_qkv"], inp["w_o"], w.H, mask_kind=w.mask_kind,
+                          rows=flat)
+    _compare(Y.reshape(-1, w.d_model)[flat], Yr, w.name)

@@ -1,0 +1,187 @@
+"""GB300-native multi-head scaled dot-product attention (forward).
+
+Thin ctypes binding of ``libgb300attn.so`` (C ABI in ``include/gb300attn.h``).
+Every step of the computation runs in the library's sm_103a kernels; this
+module only checks tensor properties and passes device pointers, sizes and
+the current CUDA stream.  PyTorch provides device memory and streams.
+
+There is no fallback: if the library has not been built, importing this
+package raises ``ImportError``.  Build it with
+``python -m transformer_scaled_dot_sdpa_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "MASK_NONE", "MASK_CAUSAL", "MASK_PADDING", "AttnError", "attn_fwd", "mha_layer_fwd",
+    "mha_layer_workspace_bytes", "gemm_bf16", "check_device_status", "set_wait_limit_ns",
+    "debug_skip_kv_load", "library_path", "lib",
+]
+
+MASK_NONE = 0
+MASK_CAUSAL = 1
+MASK_PADDING = 2
+
+ATTN_OK = 0
+STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
+                3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_TIMEOUT"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libgb300attn.so")
+
+
+class AttnError(RuntimeError):
+    """A non-OK status returned by the C library."""
+
+    def __init__(self, status: int, where: str = ""):
+        self.status = int(status)
+        super().__init__("%s%s (%d)" % (where + ": " if where else "",
+                                        STATUS_NAMES.get(self.status, "?"), self.status))
+
+
+def _load():
+    if not os.path.exists(library_path):
+        raise ImportError(
+            "libgb300attn.so is not built (expected at %s); run "
+            "`python -m transformer_scaled_dot_sdpa_gb300.build`" % library_path)
+    L = ctypes.CDLL(library_path)
+    vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float,
+                             ctypes.c_size_t)
+    L.attn_fwd.restype = i32
+    L.attn_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp, vp]
+    L.mha_layer_workspace_bytes.restype = sz
+    L.mha_layer_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.mha_layer_fwd.restype = i32
+    L.mha_layer_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, f32, vp, vp, sz, vp]
+    L.attn_gemm_bf16.restype = i32
+    L.attn_gemm_bf16.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+    L.attn_check_device_status.restype = i32
+    L.attn_check_device_status.argtypes = [vp]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_status_string.argtypes = [i32]
+    L.attn_set_wait_limit_ns.restype = None
+    L.attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    L.attn_debug_skip_kv_load.restype = None
+    L.attn_debug_skip_kv_load.argtypes = [i64]
+    return L
+
+
+lib = _load()
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(status, where):
+    if status != ATTN_OK:
+        raise AttnError(status, where)
+
+
+def _dev_tensor(t, name, dtype):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def attn_fwd(q, k, v, mask_kind=MASK_NONE, kv_lens=None, scale=None, out=None, lse=None,
+             return_lse=True, stream=None):
+    """Multi-head attention forward: softmax(Q K^T * scale + M) V.
+
+    q [B,h,Lq,d], k [B,h,Lk,d], v [B,h,Lk,d] bf16 CUDA tensors; ``kv_lens``
+    int32 [B] (padding mask); ``scale`` None -> 1/sqrt(d).  Returns
+    (O bf16 [B,h,Lq,d], LSE fp32 [B,h,Lq] or None).
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dev_tensor(t, n, torch.bfloat16)
+    B, h, Lq, dk = q.shape
+    Lk, dv = k.shape[2], v.shape[3]
+    if tuple(k.shape) != (B, h, Lk, dk) or tuple(v.shape) != (B, h, Lk, dv):
+        raise ValueError("q/k/v shapes do not match")
+    if out is None:
+        out = torch.empty((B, h, Lq, dv), dtype=torch.bfloat16, device=q.device)
+    _dev_tensor(out, "out", torch.bfloat16)
+    if tuple(out.shape) != (B, h, Lq, dv):
+        raise ValueError("out has the wrong shape")
+    if lse is None and return_lse:
+        lse = torch.empty((B, h, Lq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _dev_tensor(lse, "lse", torch.float32)
+    if kv_lens is not None:
+        _dev_tensor(kv_lens, "kv_lens", torch.int32)
+    st = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, h, Lq, Lk, dk, dv, int(mask_kind),
+                      _ptr(kv_lens), float(scale) if scale else 0.0, _ptr(out), _ptr(lse),
+                      _stream_handle(stream))
+    _check(st, "attn_fwd")
+    return out, lse
+
+
+def mha_layer_workspace_bytes(B, L, d_model, h):
+    return int(lib.mha_layer_workspace_bytes(B, L, d_model, h))
+
+
+def mha_layer_fwd(x, w_qkv, w_o, num_heads, mask_kind=MASK_NONE, kv_lens=None, scale=None,
+                  out=None, workspace=None, stream=None):
+    """Five-step multi-head layer Y = Concat_i(SDPA(X W_Q^i, X W_K^i, X W_V^i)) W_O.
+
+    x [B,L,d_model], w_qkv [d_model, 3*d_model], w_o [d_model, d_model]; bf16.
+    """
+    for t, n in ((x, "x"), (w_qkv, "w_qkv"), (w_o, "w_o")):
+        _dev_tensor(t, n, torch.bfloat16)
+    B, L, dm = x.shape
+    if out is None:
+        out = torch.empty((B, L, dm), dtype=torch.bfloat16, device=x.device)
+    _dev_tensor(out, "out", torch.bfloat16)
+    need = mha_layer_workspace_bytes(B, L, dm, num_heads)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=x.device)
+    if kv_lens is not None:
+        _dev_tensor(kv_lens, "kv_lens", torch.int32)
+    st = lib.mha_layer_fwd(_ptr(x), _ptr(w_qkv), _ptr(w_o), B, L, dm, int(num_heads),
+                           int(mask_kind), _ptr(kv_lens), float(scale) if scale else 0.0,
+                           _ptr(out), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(st, "mha_layer_fwd")
+    return out
+
+
+def gemm_bf16(a, b, out=None, stream=None):
+    """C = A B on the tensor cores (bf16 in, fp32 accumulate, bf16 out)."""
+    _dev_tensor(a, "a", torch.bfloat16)
+    _dev_tensor(b, "b", torch.bfloat16)
+    M, K = a.shape
+    if b.shape[0] != K:
+        raise ValueError("inner dimensions differ")
+    N = b.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    _dev_tensor(out, "out", torch.bfloat16)
+    st = lib.attn_gemm_bf16(_ptr(a), _ptr(b), _ptr(out), M, N, K, _stream_handle(stream))
+    _check(st, "attn_gemm_bf16")
+    return out
+
+
+def check_device_status(stream=None):
+    """Synchronize the stream and raise AttnError if a kernel reported an error."""
+    _check(lib.attn_check_device_status(_stream_handle(stream)), "device status")
+
+
+def set_wait_limit_ns(ns):
+    lib.attn_set_wait_limit_ns(int(ns))
+
+
+def debug_skip_kv_load(index):
+    lib.attn_debug_skip_kv_load(int(index))

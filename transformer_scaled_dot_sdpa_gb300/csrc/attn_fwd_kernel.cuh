@@ -1,0 +1,550 @@
+// attn_fwd_kernel.cuh -- fused multi-head scaled dot-product attention forward
+// for sm_103a (tcgen05 tensor cores, TMEM accumulators, TMA staging).
+//
+//   O = softmax(Q K^T * scale + M) V,   LSE = log(sum_j exp(scale q.k_j + M_j))
+//
+// computed one 128-query x 128-key tile at a time with the online softmax of
+// "Self-Attention 机制", section "Softmax 的数值稳定性与 Online Softmax"
+// (running row max m and running sum d, rescaled by e^(m_old - m_new) when
+// the max moves), so the n x n score matrix never leaves the chip
+// (same page, section "瓶颈：两个项，两种场景").  Under the causal mask,
+// key tiles that lie wholly above the diagonal are skipped (same page,
+// section "Causal Mask").
+//
+// CTA organisation (one CTA per SM, persistent):
+//   work item      = (batch b, head h, block of 256 query rows), taken
+//                    longest-first and dealt to CTAs in a boustrophedon order
+//   warps 0-3      = softmax group for Q tile 0 (rows 0..127 of the block)
+//   warps 4-7      = softmax group for Q tile 1 (rows 128..255)
+//   warp 8         = MMA issuer (one thread) + TMEM owner
+//   warp 9         = TMA producer (one thread)
+// TMEM (512 columns x 128 lanes, fp32):
+//   [  0,128) S of tile 0, its first 64 columns reused for P (bf16 pairs)
+//   [128,256) S / P of tile 1
+//   [256,384) O accumulator of tile 0, [384,512) O of tile 1
+// Per KV tile j the MMA thread issues S0 = Q0 K_j^T, S1 = Q1 K_j^T, then
+// O0 += P0 V_j, O1 += P1 V_j.  While one softmax group works on its S, the
+// tensor core runs the other group's GEMMs.
+//
+// Softmax state per row (one thread per row = one TMEM lane): m in log2
+// units (already multiplied by scale*log2 e) and two running sums: l of the
+// fp32 probabilities (gives the LSE) and lb of the bf16-rounded
+// probabilities that the tensor core multiplies into V (normalises O, so
+// O / lb is an exactly normalised average of V rows and a one-hot row
+// reproduces its V row).  The max used
+// for the exponentials is only moved when it grows by more than 8 (a factor
+// 256); otherwise the stale max is kept, which is exact after the final
+// division by l because O and l share it.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace gb300 {
+
+constexpr int ATTN_THREADS = 320;
+constexpr int ATTN_BLOCK_M = 128;  // query rows per Q tile
+constexpr int ATTN_BLOCK_N = 128;  // keys per KV tile
+constexpr int ATTN_QTILES = 2;     // Q tiles per work item
+constexpr int ATTN_ROWS_PER_ITEM = ATTN_BLOCK_M * ATTN_QTILES;
+constexpr uint32_t ATTN_TMEM_COLS = 512;
+constexpr float ATTN_RESCALE_THRESHOLD = 8.0f;  // log2 units
+
+enum : unsigned int { ATTN_STATUS_TIMEOUT = 1u, ATTN_STATUS_BAD_KVLEN = 2u };
+enum : int { ATTN_MASK_CAUSAL_BIT = 1, ATTN_MASK_PADDING_BIT = 2 };
+
+struct AttnParams {
+  int B, H, Lq, Lk;
+  int mask_kind;           // bit 0 causal, bit 1 padding
+  int packed;              // 0: Q/K/V maps over [B,H,L,d]; 1: over [B,L,3,H,d]
+  const int32_t* kv_lens;  // [B] valid lengths (padding) or nullptr
+  float scale_log2;        // softmax scale * log2(e)
+  __nv_bfloat16* O;
+  long long o_stride_b, o_stride_h, o_stride_l;  // in elements
+  float* LSE;              // [B,H,Lq] natural-log LSE, or nullptr
+  int n_qblocks;           // ceil(Lq / 256)
+  int n_items;             // B * H * n_qblocks
+  unsigned int* status;    // device status word
+  unsigned long long wait_limit_ns;
+  long long debug_skip_kv_load;  // test hook: skip this running K-tile load (-1: none)
+};
+
+template <int D>
+struct AttnLayout {
+  static constexpr int TILE_BYTES = ATTN_BLOCK_M * D * 2;  // 128 rows x D bf16
+  static constexpr int CHUNK_BYTES = ATTN_BLOCK_M * 128;   // 128 rows x 64 bf16
+  static constexpr int NCHUNK = D / 64;
+  static constexpr int STAGES = (D == 128) ? 2 : 4;
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + ATTN_QTILES * TILE_BYTES;
+  static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
+  static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
+  // barrier indices
+  static constexpr int B_Q_FULL = 0;
+  static constexpr int B_Q_EMPTY = 2;
+  static constexpr int B_K_FULL = 4;
+  static constexpr int B_V_FULL = B_K_FULL + STAGES;
+  static constexpr int B_KV_EMPTY = B_V_FULL + STAGES;
+  static constexpr int B_S_FULL = B_KV_EMPTY + STAGES;
+  static constexpr int B_P_FULL = B_S_FULL + 2;
+  static constexpr int B_O_DONE = B_P_FULL + 2;
+  static constexpr int B_DRAIN = B_O_DONE + 2;
+  static constexpr int N_BARS = B_DRAIN + 1;
+  static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
+  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
+};
+
+struct AttnItem {
+  int b, h;
+  int row0[ATTN_QTILES];  // first query row of each Q tile
+  int nkv[ATTN_QTILES];   // KV tiles each Q tile needs (0: nothing to compute)
+  int nkv_max;
+  int kv_len;             // valid keys of this sequence (Lk without padding)
+  int kv_len_raw;         // as given (for range reporting)
+};
+
+// Item k of this CTA.  Items are ordered heaviest first (query blocks from
+// the end of the sequence, which under the causal mask see the most keys)
+// and dealt to CTAs in a boustrophedon order, which balances the triangular
+// work without any atomics.
+__device__ __forceinline__ bool attn_get_item(const AttnParams& p, int k, AttnItem& it) {
+  const int G = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  const long long w = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
+  if (w >= p.n_items) return false;
+  const int BH = p.B * p.H;
+  const int rank = static_cast<int>(w / BH);
+  const int bh = static_cast<int>(w - static_cast<long long>(rank) * BH);
+  const int qb = p.n_qblocks - 1 - rank;
+  it.b = bh / p.H;
+  it.h = bh - it.b * p.H;
+  int kv_len = p.Lk;
+  it.kv_len_raw = p.Lk;
+  if (p.mask_kind & ATTN_MASK_PADDING_BIT) {
+    const int raw = p.kv_lens[it.b];
+    it.kv_len_raw = raw;
+    kv_len = raw < 0 ? 0 : (raw > p.Lk ? p.Lk : raw);
+  }
+  it.kv_len = kv_len;
+  it.nkv_max = 0;
+#pragma unroll
+  for (int t = 0; t < ATTN_QTILES; ++t) {
+    const int r0 = qb * ATTN_ROWS_PER_ITEM + t * ATTN_BLOCK_M;
+    it.row0[t] = r0;
+    int n = 0;
+    const bool all_padded = (p.mask_kind & ATTN_MASK_PADDING_BIT) && r0 >= kv_len;
+    if (r0 < p.Lq && !all_padded) {
+      int lim = kv_len;
+      if (p.mask_kind & ATTN_MASK_CAUSAL_BIT) {
+        const int last = min(r0 + ATTN_BLOCK_M - 1, p.Lq - 1);
+        lim = min(lim, last + 1);
+      }
+      n = (lim + ATTN_BLOCK_N - 1) / ATTN_BLOCK_N;
+    }
+    it.nkv[t] = n;
+    it.nkv_max = max(it.nkv_max, n);
+  }
+  return true;
+}
+
+__device__ __forceinline__ void attn_load_tile(const CUtensorMap* m, void* dst, uint64_t* bar,
+                                               int col, int row, int h, int b, int packed) {
+  if (packed)
+    tma_load_4d(dst, m, bar, col, h, row, b);
+  else
+    tma_load_4d(dst, m, bar, col, row, h, b);
+}
+
+// ---------------------------------------------------------------------------
+// TMA producer (one thread)
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void attn_tma_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                              const CUtensorMap* tmV, const AttnParams& p,
+                                              uint8_t* smem, uint64_t* bars, const WaitCtl& ctl) {
+  using L = AttnLayout<D>;
+  tma_prefetch_desc(tmQ);
+  tma_prefetch_desc(tmK);
+  tma_prefetch_desc(tmV);
+  uint32_t q_loads[ATTN_QTILES] = {0u, 0u};
+  uint32_t kv_it = 0;
+  bool ok = true;
+  AttnItem it;
+  for (int k = 0; ok && attn_get_item(p, k, it); ++k) {
+#pragma unroll
+    for (int t = 0; t < ATTN_QTILES; ++t) {
+      if (!ok || it.nkv[t] == 0) continue;
+      if (q_loads[t] > 0) {
+        ok = mbar_wait(&bars[L::B_Q_EMPTY + t], (q_loads[t] - 1u) & 1u, ctl);
+        if (!ok) continue;
+      }
+      mbar_arrive_expect_tx(&bars[L::B_Q_FULL + t], L::TILE_BYTES);
+      for (int c = 0; c < L::NCHUNK; ++c)
+        attn_load_tile(tmQ, smem + L::Q_OFF + t * L::TILE_BYTES + c * L::CHUNK_BYTES,
+                       &bars[L::B_Q_FULL + t], 64 * c, it.row0[t], it.h, it.b, p.packed);
+      ++q_loads[t];
+    }
+    for (int j = 0; ok && j < it.nkv_max; ++j, ++kv_it) {
+      const int s = static_cast<int>(kv_it % L::STAGES);
+      if (kv_it >= static_cast<uint32_t>(L::STAGES)) {
+        ok = mbar_wait(&bars[L::B_KV_EMPTY + s], ((kv_it / L::STAGES) - 1u) & 1u, ctl);
+        if (!ok) break;
+      }
+      if (static_cast<long long>(kv_it) != p.debug_skip_kv_load) {
+        mbar_arrive_expect_tx(&bars[L::B_K_FULL + s], L::TILE_BYTES);
+        for (int c = 0; c < L::NCHUNK; ++c)
+          attn_load_tile(tmK, smem + L::K_OFF + s * L::TILE_BYTES + c * L::CHUNK_BYTES,
+                         &bars[L::B_K_FULL + s], 64 * c, j * ATTN_BLOCK_N, it.h, it.b, p.packed);
+      }
+      mbar_arrive_expect_tx(&bars[L::B_V_FULL + s], L::TILE_BYTES);
+      for (int c = 0; c < L::NCHUNK; ++c)
+        attn_load_tile(tmV, smem + L::V_OFF + s * L::TILE_BYTES + c * L::CHUNK_BYTES,
+                       &bars[L::B_V_FULL + s], 64 * c, j * ATTN_BLOCK_N, it.h, it.b, p.packed);
+    }
+  }
+  // Unwind: every load this thread issued must land before the CTA exits.
+  // On the normal path these phases completed long ago.
+  for (int t = 0; t < ATTN_QTILES; ++t)
+    if (q_loads[t] > 0)
+      mbar_wait_drain(&bars[L::B_Q_FULL + t], (q_loads[t] - 1u) & 1u, ctl.limit_ns);
+  for (int s = 0; s < L::STAGES; ++s) {
+    if (kv_it <= static_cast<uint32_t>(s)) continue;
+    const uint32_t n_s = (kv_it - s + L::STAGES - 1) / L::STAGES;  // loads into stage s
+    const uint32_t last = s + (n_s - 1u) * L::STAGES;                 // running index
+    if (static_cast<long long>(last) != p.debug_skip_kv_load)
+      mbar_wait_drain(&bars[L::B_K_FULL + s], (n_s - 1u) & 1u, ctl.limit_ns);
+    mbar_wait_drain(&bars[L::B_V_FULL + s], (n_s - 1u) & 1u, ctl.limit_ns);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (one thread)
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void attn_mma_role(const AttnParams& p, uint8_t* smem, uint64_t* bars,
+                                              uint32_t tmem, const WaitCtl& ctl) {
+  using L = AttnLayout<D>;
+  constexpr uint32_t IDESC_S = idesc_bf16_f32(ATTN_BLOCK_M, ATTN_BLOCK_N, false);
+  constexpr uint32_t IDESC_O = idesc_bf16_f32(ATTN_BLOCK_M, D, true);
+  const uint32_t q_base = smem_u32(smem + L::Q_OFF);
+  const uint32_t k_base = smem_u32(smem + L::K_OFF);
+  const uint32_t v_base = smem_u32(smem + L::V_OFF);
+  uint32_t q_uses[ATTN_QTILES] = {0u, 0u};
+  uint32_t p_cnt[ATTN_QTILES] = {0u, 0u};
+  uint32_t pv_cnt[ATTN_QTILES] = {0u, 0u};
+  uint32_t kv_it = 0;
+  bool ok = true;
+  AttnItem it;
+  for (int k = 0; ok && attn_get_item(p, k, it); ++k) {
+    if (it.kv_len_raw != it.kv_len) atomicOr(p.status, ATTN_STATUS_BAD_KVLEN);
+#pragma unroll
+    for (int t = 0; t < ATTN_QTILES; ++t) {
+      if (ok && it.nkv[t] > 0) {
+        ok = mbar_wait(&bars[L::B_Q_FULL + t], q_uses[t] & 1u, ctl);
+        ++q_uses[t];
+      }
+    }
+    for (int j = 0; ok && j < it.nkv_max; ++j, ++kv_it) {
+      const int s = static_cast<int>(kv_it % L::STAGES);
+      const uint32_t ph = (kv_it / L::STAGES) & 1u;
+      ok = mbar_wait(&bars[L::B_K_FULL + s], ph, ctl);
+      // S_t = Q_t K_j^T for both Q tiles
+#pragma unroll
+      for (int t = 0; t < ATTN_QTILES; ++t) {
+        if (!ok || j >= it.nkv[t]) continue;
+        // S_t's columns still hold P_t of the previous tile until that P.V is done
+        if (pv_cnt[t] > 0) ok = mbar_wait(&bars[L::B_O_DONE + t], (pv_cnt[t] - 1u) & 1u, ctl);
+        if (!ok) continue;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(t * ATTN_BLOCK_N);
+        const uint32_t qa = q_base + t * L::TILE_BYTES;
+        const uint32_t ka = k_base + s * L::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::CHUNK_BYTES + (kk & 3) * 32;
+          mma_bf16_ss(d_tmem, smem_desc_sw128(qa + off, 16, 1024),
+                      smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars[L::B_S_FULL + t]);
+        if (j == it.nkv[t] - 1) mma_commit(&bars[L::B_Q_EMPTY + t]);
+      }
+      if (!ok) break;
+      ok = mbar_wait(&bars[L::B_V_FULL + s], ph, ctl);
+      // O_t += P_t V_j
+#pragma unroll
+      for (int t = 0; t < ATTN_QTILES; ++t) {
+        if (!ok || j >= it.nkv[t]) continue;
+        ok = mbar_wait(&bars[L::B_P_FULL + t], p_cnt[t] & 1u, ctl);
+        if (!ok) continue;
+        ++p_cnt[t];
+        tc_fence_after();
+        const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(t * 128);
+        const uint32_t p_tmem = tmem + static_cast<uint32_t>(t * ATTN_BLOCK_N);
+        const uint32_t va = v_base + s * L::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < ATTN_BLOCK_N / 16; ++kk) {
+          mma_bf16_ts(o_tmem, p_tmem + kk * 8, smem_desc_sw128(va + kk * 2048, L::CHUNK_BYTES, 1024),
+                      IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bars[L::B_O_DONE + t]);
+        ++pv_cnt[t];
+      }
+      if (!ok) break;
+      mma_commit(&bars[L::B_KV_EMPTY + s]);
+    }
+  }
+  // Unwind: all MMAs issued by this thread complete before TMEM is freed.
+  mma_commit(&bars[L::B_DRAIN]);
+  mbar_wait_drain(&bars[L::B_DRAIN], 0u, ctl.limit_ns);
+}
+
+// ---------------------------------------------------------------------------
+// softmax / correction / epilogue group (128 threads, one query row each)
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams& p,
+                                                  uint64_t* bars, uint32_t tmem,
+                                                  const WaitCtl& ctl) {
+  using L = AttnLayout<D>;
+  const int rloc = static_cast<int>(threadIdx.x & 127u);
+  const uint32_t lane_base = static_cast<uint32_t>(threadIdx.x & 96u) << 16;
+  const uint32_t s_tmem = tmem + static_cast<uint32_t>(t * ATTN_BLOCK_N) + lane_base;
+  const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(t * 128) + lane_base;
+  const float c = p.scale_log2;
+  const bool causal = (p.mask_kind & ATTN_MASK_CAUSAL_BIT) != 0;
+  const bool padding = (p.mask_kind & ATTN_MASK_PADDING_BIT) != 0;
+  uint32_t s_cnt = 0, pv_cnt = 0;
+  bool ok = true;
+  AttnItem it;
+  for (int k = 0; ok && attn_get_item(p, k, it); ++k) {
+    const int row0 = t ? it.row0[1] : it.row0[0];
+    const int nkv = t ? it.nkv[1] : it.nkv[0];
+    if (row0 >= p.Lq) continue;  // tile wholly past the end of the sequence
+    const int r = row0 + rloc;
+    int limit = it.kv_len;  // this row attends to keys [0, limit)
+    if (causal) limit = min(limit, r + 1);
+    const bool padded_row = padding && r >= it.kv_len;
+    float m = -INFINITY, l = 0.f, lb = 0.f;
+    for (int j = 0; j < nkv; ++j) {
+      ok = mbar_wait(&bars[L::B_S_FULL + t], s_cnt & 1u, ctl);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ++s_cnt;
+      tc_fence_after();
+      uint32_t ra[32], rb[32], rc[32], rd[32];
+      tmem_ld_32x32b_x32(s_tmem + 0u, ra);
+      tmem_ld_32x32b_x32(s_tmem + 32u, rb);
+      tmem_ld_32x32b_x32(s_tmem + 64u, rc);
+      tmem_ld_32x32b_x32(s_tmem + 96u, rd);
+      tmem_ld_wait(ra);
+      reg_fence(rb);
+      reg_fence(rc);
+      reg_fence(rd);
+      float s[128];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        s[i] = __uint_as_float(ra[i]);
+        s[32 + i] = __uint_as_float(rb[i]);
+        s[64 + i] = __uint_as_float(rc[i]);
+        s[96 + i] = __uint_as_float(rd[i]);
+      }
+      // mask: keys at or past `limit` (causal diagonal, padding, end of keys)
+      const int nvalid = limit - j * ATTN_BLOCK_N;
+      if (nvalid < ATTN_BLOCK_N) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = (i < nvalid) ? s[i] : -INFINITY;
+      }
+      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
+#pragma unroll
+      for (int i = 4; i < 128; i += 4) {
+        mx0 = fmax3(mx0, s[i], s[i + 1]);
+        mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
+      }
+      const float mx = fmaxf(mx0, mx1);
+      const float m_tile = mx * c;  // scale > 0, so the max commutes with it
+      const float m_new = fmaxf(m, m_tile);
+      const bool need = m_new > m + ATTN_RESCALE_THRESHOLD;
+      if (__any_sync(0xffffffffu, need && j > 0)) {
+        // rescale this row's O accumulator; the previous P.V must be done
+        ok = mbar_wait(&bars[L::B_O_DONE + t], (pv_cnt - 1u) & 1u, ctl);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t ro[32];
+          tmem_ld_32x32b_x32(o_tmem + cc * 32u, ro);
+          tmem_ld_wait(ro);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
+          tmem_st_32x32b_x32(o_tmem + cc * 32u, ro);
+        }
+        tmem_st_wait();
+      }
+      if (need) {
+        const float alpha = ex2_approx(m - m_new);
+        l *= alpha;
+        lb *= alpha;
+        m = m_new;
+      }
+      const float mb = (m == -INFINITY) ? 0.f : m;
+      // p = 2^(s*c - m); P goes to TMEM as bf16 pairs.  Two row sums: lf of
+      // the fp32 p (for the LSE) and lb of the bf16-rounded p that the tensor
+      // core multiplies into V (for the normalisation of O).
+      const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-mb, -mb);
+      uint64_t lf2 = 0ull, lb2 = 0ull;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float a0, a1;
+          f2_unpack(f2_fma(f2_pack(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]), c2, nm2), a0,
+                    a1);
+          const float p0 = ex2_approx(a0);
+          const float p1 = ex2_approx(a1);
+          pk[i] = pack_bf16x2(p0, p1);
+          lf2 = f2_add(lf2, f2_pack(p0, p1));
+          lb2 = f2_add(lb2, f2_pack(bf16x2_lo(pk[i]), bf16x2_hi(pk[i])));
+        }
+        tmem_st_32x32b_x32(s_tmem + 32u * half, pk);
+        tmem_st_wait();
+      }
+      {
+        float x0, x1, y0, y1;
+        f2_unpack(lf2, x0, x1);
+        f2_unpack(lb2, y0, y1);
+        l += x0 + x1;
+        lb += y0 + y1;
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[L::B_P_FULL + t]);
+      ++pv_cnt;
+    }
+    if (!ok) break;
+    // epilogue: O / l (bf16), LSE; padded and empty rows are exactly 0 / -inf
+    if (nkv > 0) {
+      ok = mbar_wait(&bars[L::B_O_DONE + t], (pv_cnt - 1u) & 1u, ctl);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+    }
+    const bool in_range = r < p.Lq;
+    const bool zero_row = padded_row || nkv == 0 || limit <= 0 || !(lb > 0.f);
+    const float inv_l = zero_row ? 0.f : 1.0f / lb;
+    __nv_bfloat16* orow = p.O + it.b * p.o_stride_b + it.h * p.o_stride_h +
+                          static_cast<long long>(r) * p.o_stride_l;
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) {
+      uint32_t ro[32];
+      if (nkv > 0) {
+        tmem_ld_32x32b_x32(o_tmem + cc * 32u, ro);
+        tmem_ld_wait(ro);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ro[i] = 0u;
+      }
+      if (in_range) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = zero_row ? 0u
+                          : pack_bf16x2(__uint_as_float(ro[2 * i]) * inv_l,
+                                        __uint_as_float(ro[2 * i + 1]) * inv_l);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          st_global_v4(orow + cc * 32 + i * 8, w[4 * i], w[4 * i + 1], w[4 * i + 2],
+                       w[4 * i + 3]);
+      }
+    }
+    if (p.LSE != nullptr && in_range) {
+      const float lse = zero_row ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
+      p.LSE[(static_cast<long long>(it.b) * p.H + it.h) * p.Lq + r] = lse;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(ATTN_THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using L = AttnLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~static_cast<uintptr_t>(1023u));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  const int lane = static_cast<int>(threadIdx.x & 31u);
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < ATTN_QTILES; ++t) {
+      mbar_init(&bars[L::B_Q_FULL + t], 1);
+      mbar_init(&bars[L::B_Q_EMPTY + t], 1);
+      mbar_init(&bars[L::B_S_FULL + t], 1);
+      mbar_init(&bars[L::B_P_FULL + t], 128);
+      mbar_init(&bars[L::B_O_DONE + t], 1);
+    }
+    for (int s = 0; s < L::STAGES; ++s) {
+      mbar_init(&bars[L::B_K_FULL + s], 1);
+      mbar_init(&bars[L::B_V_FULL + s], 1);
+      mbar_init(&bars[L::B_KV_EMPTY + s], 1);
+    }
+    mbar_init(&bars[L::B_DRAIN], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, ATTN_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns, ATTN_STATUS_TIMEOUT};
+
+  if (warp == 9) {
+    if (lane == 0) attn_tma_role<D>(&tmQ, &tmK, &tmV, p, smem, bars, ctl);
+  } else if (warp == 8) {
+    if (lane == 0) attn_mma_role<D>(p, smem, bars, tmem, ctl);
+    __syncwarp();
+  } else {
+    attn_softmax_role<D>(warp >> 2, p, bars, tmem, ctl);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ATTN_TMEM_COLS);
+  }
+}
+
+// Output for sequences with no keys at all (Lk == 0): O = 0, LSE = -inf.
+__global__ void attn_empty_keys_kernel(__nv_bfloat16* O, long long o_stride_b,
+                                       long long o_stride_h, long long o_stride_l, float* LSE,
+                                       int B, int H, int Lq, int D) {
+  const long long rows = static_cast<long long>(B) * H * Lq;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < rows * D;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = i / D;
+    const int col = static_cast<int>(i - row * D);
+    const int r = static_cast<int>(row % Lq);
+    const long long bh = row / Lq;
+    const int h = static_cast<int>(bh % H);
+    const int b = static_cast<int>(bh / H);
+    O[b * o_stride_b + h * o_stride_h + static_cast<long long>(r) * o_stride_l + col] =
+        __float2bfloat16(0.f);
+    if (col == 0 && LSE != nullptr) LSE[row] = -INFINITY;
+  }
+}
+
+}  // namespace gb300

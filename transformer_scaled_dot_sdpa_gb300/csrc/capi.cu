@@ -1,0 +1,365 @@
+// capi.cu -- host side of libgb300attn.so: argument validation, TMA tensor
+// maps, kernel launch, and the device status word.  See include/gb300attn.h
+// for the contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gb300attn.h"
+#include "attn_fwd_kernel.cuh"
+#include "gemm_kernel.cuh"
+
+namespace {
+
+// Device status word: bits set by kernels (timeout, bad kv_len), read and
+// cleared by attn_check_device_status().  One copy per device.
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  unsigned int* status = nullptr;
+  bool attn_attr[2] = {false, false};
+  bool gemm_attr = false;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+unsigned long long g_wait_limit_ns = kDefaultWaitLimitNs;
+long long g_debug_skip_kv_load = -1;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+attn_status_t get_encode() {
+  if (g_encode) return ATTN_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return ATTN_ERR_CUDA;
+  g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  return ATTN_OK;
+}
+
+// Per-device state for the current device (lazily initialised).
+attn_status_t device_state(DeviceState** out, int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;  // built for sm_103a only
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return ATTN_ERR_CUDA;
+    s.status = static_cast<unsigned int*>(p);
+    if (get_encode() != ATTN_OK) return ATTN_ERR_CUDA;
+    s.ready = true;
+  }
+  *out = &s;
+  if (dev_out) *dev_out = dev;
+  return ATTN_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// 4-D bf16 tensor map with a 64 x 128 box (the 128-row dimension is `row_dim`),
+// 128-byte swizzle, zero fill out of bounds.
+attn_status_t make_map_4d(CUtensorMap* m, const void* base, const cuuint64_t dims[4],
+                          const cuuint64_t strides_bytes[3], const cuuint32_t box[4]) {
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Tensor map over a contiguous [B, H, L, d] bf16 tensor.
+attn_status_t map_bhld(CUtensorMap* m, const void* base, int B, int H, int L, int d) {
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)L, (cuuint64_t)H, (cuuint64_t)B};
+  const cuuint64_t str[3] = {(cuuint64_t)d * 2, (cuuint64_t)L * d * 2,
+                             (cuuint64_t)H * L * d * 2};
+  const cuuint32_t box[4] = {64, 128, 1, 1};
+  return make_map_4d(m, base, dims, str, box);
+}
+
+// Tensor map over one of the Q/K/V blocks of a packed [B, L, 3, H, d] tensor
+// (base already offset to the block); dimension order (d, H, L, B).
+attn_status_t map_packed(CUtensorMap* m, const void* base, int B, int H, int L, int d) {
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
+  const cuuint64_t str[3] = {(cuuint64_t)d * 2, (cuuint64_t)3 * H * d * 2,
+                             (cuuint64_t)L * 3 * H * d * 2};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  return make_map_4d(m, base, dims, str, box);
+}
+
+template <int D>
+attn_status_t launch_attn(DeviceState* ds, int attr_idx, const CUtensorMap& mq,
+                          const CUtensorMap& mk, const CUtensorMap& mv, const gb300::AttnParams& p,
+                          cudaStream_t stream) {
+  using L = gb300::AttnLayout<D>;
+  if (!ds->attn_attr[attr_idx]) {
+    if (cudaFuncSetAttribute(gb300::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::SMEM_BYTES) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    ds->attn_attr[attr_idx] = true;
+  }
+  const int grid = p.n_items < ds->num_sms ? p.n_items : ds->num_sms;
+  gb300::attn_fwd_kernel<D><<<grid, gb300::ATTN_THREADS, L::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Shared by attn_fwd and the layer: launch attention with prepared maps.
+attn_status_t run_attention(DeviceState* ds, const CUtensorMap& mq, const CUtensorMap& mk,
+                            const CUtensorMap& mv, int packed, int B, int H, int Lq, int Lk,
+                            int d, int mask_kind, const int32_t* kv_lens, float scale, void* O,
+                            long long osb, long long osh, long long osl, float* LSE,
+                            cudaStream_t stream) {
+  gb300::AttnParams p;
+  std::memset(&p, 0, sizeof p);
+  p.B = B;
+  p.H = H;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.mask_kind = mask_kind;
+  p.packed = packed;
+  p.kv_lens = kv_lens;
+  const double sc = scale > 0.f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(d));
+  p.scale_log2 = static_cast<float>(sc * 1.4426950408889634074);
+  p.O = static_cast<__nv_bfloat16*>(O);
+  p.o_stride_b = osb;
+  p.o_stride_h = osh;
+  p.o_stride_l = osl;
+  p.LSE = LSE;
+  p.n_qblocks = (Lq + gb300::ATTN_ROWS_PER_ITEM - 1) / gb300::ATTN_ROWS_PER_ITEM;
+  p.n_items = static_cast<int>(static_cast<long long>(B) * H * p.n_qblocks);
+  p.status = ds->status;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    p.wait_limit_ns = g_wait_limit_ns;
+    p.debug_skip_kv_load = g_debug_skip_kv_load;
+  }
+  if (d == 64) return launch_attn<64>(ds, 0, mq, mk, mv, p, stream);
+  return launch_attn<128>(ds, 1, mq, mk, mv, p, stream);
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box cols_box x rows_box.
+attn_status_t map_2d(CUtensorMap* m, const void* base, int rows, int cols, int cols_box,
+                     int rows_box) {
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t str[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)cols_box, (cuuint32_t)rows_box};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        str, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// C[M,N] = A[M,K] B[K,N]; sizes already validated.
+attn_status_t run_gemm(DeviceState* ds, const void* A, const void* Bm, void* C, int M, int N,
+                       int K, cudaStream_t stream) {
+  CUtensorMap ma, mb;
+  attn_status_t st;
+  if ((st = map_2d(&ma, A, M, K, gb300::GEMM_BK, gb300::GEMM_BM)) != ATTN_OK) return st;
+  if ((st = map_2d(&mb, Bm, K, N, 64, gb300::GEMM_BK)) != ATTN_OK) return st;
+  if (!ds->gemm_attr) {
+    if (cudaFuncSetAttribute(gb300::gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gb300::GemmLayout::SMEM_BYTES) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    ds->gemm_attr = true;
+  }
+  gb300::GemmParams p;
+  std::memset(&p, 0, sizeof p);
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.m_tiles = M / gb300::GEMM_BM;
+  p.n_tiles = N / gb300::GEMM_BN;
+  p.k_blocks = K / gb300::GEMM_BK;
+  p.C = static_cast<__nv_bfloat16*>(C);
+  p.status = ds->status;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    p.wait_limit_ns = g_wait_limit_ns;
+  }
+  const int tiles = p.m_tiles * p.n_tiles;
+  const int grid = tiles < ds->num_sms ? tiles : ds->num_sms;
+  gb300::gemm_bf16_kernel<<<grid, gb300::GEMM_THREADS, gb300::GemmLayout::SMEM_BYTES, stream>>>(
+      ma, mb, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+  }
+  return "ATTN_STATUS_UNKNOWN";
+}
+
+void attn_set_wait_limit_ns(uint64_t ns) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_wait_limit_ns = ns ? static_cast<unsigned long long>(ns) : kDefaultWaitLimitNs;
+}
+
+void attn_debug_skip_kv_load(long long index) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_debug_skip_kv_load = index < 0 ? -1 : index;
+}
+
+attn_status_t attn_fwd(const void* Q, const void* K, const void* V, int B, int h, int Lq, int Lk,
+                       int d_k, int d_v, int mask_kind, const int32_t* kv_lens, float scale,
+                       void* O, float* LSE, void* stream) {
+  // ---- host-side validation (no CUDA call before this point) ----
+  if (B < 0 || h < 0 || Lq < 0 || Lk < 0) return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_PADDING)) != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale == scale) || std::isinf(scale)) return ATTN_ERR_INVALID_ARG;
+  if (d_k != d_v) return ATTN_ERR_UNSUPPORTED;
+  if (d_k != 64 && d_k != 128) return ATTN_ERR_UNSUPPORTED;
+  const long long n_qblocks = (static_cast<long long>(Lq) + gb300::ATTN_ROWS_PER_ITEM - 1) /
+                              gb300::ATTN_ROWS_PER_ITEM;
+  if (static_cast<long long>(B) * h * n_qblocks >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || h == 0 || Lq == 0) return ATTN_OK;
+  if (!O) return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ATTN_MASK_PADDING) && !kv_lens) return ATTN_ERR_INVALID_ARG;
+  if (Lk > 0 && (!Q || !K || !V)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(O, 16) || (LSE && !aligned(LSE, 4)) || (kv_lens && !aligned(kv_lens, 4)))
+    return ATTN_ERR_MISALIGNED;
+  if (Lk > 0 && (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16)))
+    return ATTN_ERR_MISALIGNED;
+
+  DeviceState* ds = nullptr;
+  attn_status_t st = device_state(&ds, nullptr);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long osl = d_v, osh = static_cast<long long>(Lq) * d_v, osb = osh * h;
+  if (Lk == 0) {
+    gb300::attn_empty_keys_kernel<<<256, 256, 0, s>>>(static_cast<__nv_bfloat16*>(O), osb, osh,
+                                                     osl, LSE, B, h, Lq, d_v);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+  CUtensorMap mq, mk, mv;
+  if ((st = map_bhld(&mq, Q, B, h, Lq, d_k)) != ATTN_OK) return st;
+  if ((st = map_bhld(&mk, K, B, h, Lk, d_k)) != ATTN_OK) return st;
+  if ((st = map_bhld(&mv, V, B, h, Lk, d_v)) != ATTN_OK) return st;
+  return run_attention(ds, mq, mk, mv, 0, B, h, Lq, Lk, d_k, mask_kind, kv_lens, scale, O, osb,
+                       osh, osl, LSE, s);
+}
+
+size_t mha_layer_workspace_bytes(int B, int L, int d_model, int h) {
+  if (B <= 0 || L <= 0 || d_model <= 0 || h <= 0 || d_model % h != 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * L;
+  const size_t qkv = rows * 3 * d_model * 2;
+  const size_t cat = rows * d_model * 2;
+  const size_t qkv_aligned = (qkv + 255) & ~static_cast<size_t>(255);
+  return qkv_aligned + cat;
+}
+
+attn_status_t attn_gemm_bf16(const void* A, const void* Bm, void* C, int M, int N, int K,
+                             void* stream) {
+  if (M < 0 || N < 0 || K < 0) return ATTN_ERR_INVALID_ARG;
+  if (M % gb300::GEMM_BM != 0 || N % gb300::GEMM_BN != 0 || K % gb300::GEMM_BK != 0)
+    return ATTN_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return ATTN_OK;
+  if (K == 0) return ATTN_ERR_UNSUPPORTED;
+  if (!A || !Bm || !C) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(Bm, 16) || !aligned(C, 16)) return ATTN_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  attn_status_t st = device_state(&ds, nullptr);
+  if (st != ATTN_OK) return st;
+  return run_gemm(ds, A, Bm, C, M, N, K, static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t mha_layer_fwd(const void* X, const void* W_QKV, const void* W_O, int B, int L,
+                            int d_model, int h, int mask_kind, const int32_t* kv_lens,
+                            float scale, void* Y, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (B < 0 || L < 0 || d_model <= 0 || h <= 0) return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_PADDING)) != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale == scale) || std::isinf(scale)) return ATTN_ERR_INVALID_ARG;
+  if (d_model % h != 0) return ATTN_ERR_INVALID_ARG;
+  const int dk = d_model / h;
+  if (dk != 64 && dk != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d_model % gb300::GEMM_BN != 0) return ATTN_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(B) * L;
+  if (rows % gb300::GEMM_BM != 0 || rows >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  if (rows == 0) return ATTN_OK;
+  if (!X || !W_QKV || !W_O || !Y || !workspace) return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ATTN_MASK_PADDING) && !kv_lens) return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < mha_layer_workspace_bytes(B, L, d_model, h)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(X, 16) || !aligned(W_QKV, 16) || !aligned(W_O, 16) || !aligned(Y, 16) ||
+      !aligned(workspace, 256) || (kv_lens && !aligned(kv_lens, 4)))
+    return ATTN_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  attn_status_t st = device_state(&ds, nullptr);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t qkv_bytes = static_cast<size_t>(rows) * 3 * d_model * 2;
+  uint8_t* qkv = ws;
+  uint8_t* cat = ws + ((qkv_bytes + 255) & ~static_cast<size_t>(255));
+  // step 1: QKV = X W_QKV  -> [B, L, 3, h, d_k]
+  if ((st = run_gemm(ds, X, W_QKV, qkv, static_cast<int>(rows), 3 * d_model, d_model, s)) !=
+      ATTN_OK)
+    return st;
+  // steps 2-4: split heads (strided tensor maps), attention, concat (strided store)
+  CUtensorMap mq, mk, mv;
+  const size_t blk = static_cast<size_t>(d_model) * 2;
+  if ((st = map_packed(&mq, qkv, B, h, L, dk)) != ATTN_OK) return st;
+  if ((st = map_packed(&mk, qkv + blk, B, h, L, dk)) != ATTN_OK) return st;
+  if ((st = map_packed(&mv, qkv + 2 * blk, B, h, L, dk)) != ATTN_OK) return st;
+  if ((st = run_attention(ds, mq, mk, mv, 1, B, h, L, L, dk, mask_kind, kv_lens, scale, cat,
+                          static_cast<long long>(L) * d_model, dk, d_model, nullptr, s)) !=
+      ATTN_OK)
+    return st;
+  // step 5: Y = Concat W_O
+  return run_gemm(ds, cat, W_O, Y, static_cast<int>(rows), d_model, d_model, s);
+}
+
+attn_status_t attn_check_device_status(void* stream) {
+  DeviceState* ds = nullptr;
+  attn_status_t st = device_state(&ds, nullptr);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, ds->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (word != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(ds->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  if (word & gb300::ATTN_STATUS_TIMEOUT) return ATTN_ERR_TIMEOUT;
+  if (word & gb300::ATTN_STATUS_BAD_KVLEN) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+}  // extern "C"
