@@ -47,7 +47,9 @@ typedef enum {
   ATTN_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement  */
   ATTN_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned            */
   ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed            */
-  ATTN_ERR_TIMEOUT = 5       /* a device-side pipeline wait gave up          */
+  ATTN_ERR_TIMEOUT = 5,      /* a device-side pipeline wait gave up          */
+  ATTN_ERR_TOO_LARGE = 6     /* problem exceeds the fixed scratch of
+                                mha_layer_fwd_noalloc                       */
 } attn_status_t;
 
 /* mask_kind bit flags; ATTN_MASK_CAUSAL | ATTN_MASK_PADDING applies both */
@@ -108,6 +110,40 @@ attn_status_t mha_layer_fwd(const void* X, const void* W_QKV, const void* W_O, i
                             int d_model, int h, int mask_kind, const int32_t* kv_lens,
                             float scale, void* Y, void* workspace, size_t workspace_bytes,
                             void* stream);
+
+/*
+ * mha_layer_fwd_noalloc -- the same five-step layer as mha_layer_fwd, for
+ * callers that may not allocate device memory: for example a plugin inside a
+ * host framework that owns every device buffer through its own pool and does
+ * not let plugins call cudaMalloc, or a runtime whose memory plan is fixed at
+ * start-up (cudaMalloc can stall the whole device and can fail under memory
+ * pressure, which such a runtime cannot afford in the middle of a run).  The
+ * tutorial pages have no counterpart to this entry point; it only changes
+ * where the layer's scratch lives.
+ *
+ * The caller still passes X, W_QKV, W_O, Y (and kv_lens) exactly as for
+ * mha_layer_fwd.  The scratch (the QKV projection and the concatenated heads,
+ * mha_layer_workspace_bytes() bytes) comes from one fixed array of
+ * ATTN_NOALLOC_SCRATCH_BYTES (32 MiB) compiled into the library: every GPU on
+ * which the library is loaded holds that array until the process exits.
+ * Nothing is allocated or freed by the call.
+ *   - A shape whose workspace exceeds ATTN_NOALLOC_SCRATCH_BYTES is rejected
+ *     with ATTN_ERR_TOO_LARGE before anything is launched (for d_model = 1024
+ *     the limit is B*L <= 4096 tokens).
+ *   - The first call on a device looks up the array's device address (a
+ *     cudaGetSymbolAddress on the current device); make that first call before
+ *     any stream capture.
+ *   - Every call on a device shares the one array, which keeps whatever the
+ *     last call left in it; the layer overwrites all of the scratch it reads,
+ *     so nothing needs clearing.  Calls whose execution overlaps on the GPU
+ *     (e.g. on two streams without ordering between them) race on the array
+ *     and give wrong results: order them.
+ * Returns and validation otherwise as for mha_layer_fwd.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+attn_status_t mha_layer_fwd_noalloc(const void* X, const void* W_QKV, const void* W_O, int B,
+                                    int L, int d_model, int h, int mask_kind,
+                                    const int32_t* kv_lens, float scale, void* Y, void* stream);
 
 /*
  * attn_gemm_bf16 -- C = A B with bf16 inputs, fp32 accumulation and bf16

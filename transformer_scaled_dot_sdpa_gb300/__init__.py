@@ -7,7 +7,7 @@ the current CUDA stream.  PyTorch provides device memory and streams.
 
 There is no fallback: if the library has not been built, importing this
 package raises ``ImportError``.  Build it with
-``python -m transformer_scaled_dot_sdpa_gb300.build`` (or
+``python transformer_scaled_dot_sdpa_gb300/build.py`` (or
 ``__graft_entry__.build()``).
 """
 from __future__ import annotations
@@ -19,7 +19,8 @@ import torch
 
 __all__ = [
     "MASK_NONE", "MASK_CAUSAL", "MASK_PADDING", "AttnError", "attn_fwd", "mha_layer_fwd",
-    "mha_layer_workspace_bytes", "gemm_bf16", "check_device_status", "set_wait_limit_ns",
+    "mha_layer_workspace_bytes", "mha_layer_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gemm_bf16",
+    "check_device_status", "set_wait_limit_ns",
     "debug_skip_kv_load", "library_path", "lib",
 ]
 
@@ -29,7 +30,9 @@ MASK_PADDING = 2
 
 ATTN_OK = 0
 STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
-                3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_TIMEOUT"}
+                3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_TIMEOUT",
+                6: "ATTN_ERR_TOO_LARGE"}
+NOALLOC_SCRATCH_BYTES = 32 << 20  # ATTN_NOALLOC_SCRATCH_BYTES
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libgb300attn.so")
@@ -48,7 +51,7 @@ def _load():
     if not os.path.exists(library_path):
         raise ImportError(
             "libgb300attn.so is not built (expected at %s); run "
-            "`python -m transformer_scaled_dot_sdpa_gb300.build`" % library_path)
+            "`python transformer_scaled_dot_sdpa_gb300/build.py`" % library_path)
     L = ctypes.CDLL(library_path)
     vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float,
                              ctypes.c_size_t)
@@ -58,6 +61,8 @@ def _load():
     L.mha_layer_workspace_bytes.argtypes = [i32, i32, i32, i32]
     L.mha_layer_fwd.restype = i32
     L.mha_layer_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, f32, vp, vp, sz, vp]
+    L.mha_layer_fwd_noalloc.restype = i32
+    L.mha_layer_fwd_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, f32, vp, vp]
     L.attn_gemm_bf16.restype = i32
     L.attn_gemm_bf16.argtypes = [vp, vp, vp, i32, i32, i32, vp]
     L.attn_check_device_status.restype = i32
@@ -155,6 +160,30 @@ def mha_layer_fwd(x, w_qkv, w_o, num_heads, mask_kind=MASK_NONE, kv_lens=None, s
                            int(mask_kind), _ptr(kv_lens), float(scale) if scale else 0.0,
                            _ptr(out), _ptr(workspace), workspace.numel(), _stream_handle(stream))
     _check(st, "mha_layer_fwd")
+    return out
+
+
+def mha_layer_fwd_noalloc(x, w_qkv, w_o, num_heads, mask_kind=MASK_NONE, kv_lens=None,
+                          scale=None, out=None, stream=None):
+    """The five-step layer with its scratch in the library's fixed device
+    array (no device allocation by the library).  For callers that may not
+    allocate device memory (a plugin whose host framework owns all device
+    buffers, a runtime with a memory plan fixed at start-up).  Shapes whose
+    scratch exceeds NOALLOC_SCRATCH_BYTES raise AttnError(ATTN_ERR_TOO_LARGE);
+    calls that overlap on the GPU share the array and must be ordered.
+    ``out`` must be given by callers that cannot allocate."""
+    for t, n in ((x, "x"), (w_qkv, "w_qkv"), (w_o, "w_o")):
+        _dev_tensor(t, n, torch.bfloat16)
+    B, L, dm = x.shape
+    if out is None:
+        out = torch.empty((B, L, dm), dtype=torch.bfloat16, device=x.device)
+    _dev_tensor(out, "out", torch.bfloat16)
+    if kv_lens is not None:
+        _dev_tensor(kv_lens, "kv_lens", torch.int32)
+    st = lib.mha_layer_fwd_noalloc(_ptr(x), _ptr(w_qkv), _ptr(w_o), B, L, dm, int(num_heads),
+                                   int(mask_kind), _ptr(kv_lens), float(scale) if scale else 0.0,
+                                   _ptr(out), _stream_handle(stream))
+    _check(st, "mha_layer_fwd_noalloc")
     return out
 
 

@@ -1,6 +1,6 @@
 """Build libgb300attn.so in-tree with nvcc (sm_103a only).
 
-    python -m transformer_scaled_dot_sdpa_gb300.build [--verbose]
+    python transformer_scaled_dot_sdpa_gb300/build.py [--verbose]
 """
 from __future__ import annotations
 

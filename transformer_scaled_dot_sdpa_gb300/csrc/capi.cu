@@ -19,6 +19,12 @@ namespace {
 // cleared by attn_check_device_status().  One copy per device.
 __device__ unsigned int g_status_word;
 
+// Fixed scratch of mha_layer_fwd_noalloc (the layer's QKV projection and
+// concatenated heads), for callers that cannot allocate device memory.  Host
+// code must not use this name as a device pointer: the device address comes
+// from cudaGetSymbolAddress (see noalloc_scratch_address).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
+
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
 
@@ -28,6 +34,7 @@ struct DeviceState {
   unsigned int* status = nullptr;
   bool attn_attr[2] = {false, false};
   bool gemm_attr = false;
+  void* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch
 };
 
 std::mutex g_mutex;
@@ -220,6 +227,7 @@ const char* attn_status_string(attn_status_t s) {
     case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED";
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
     case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    case ATTN_ERR_TOO_LARGE: return "ATTN_ERR_TOO_LARGE";
   }
   return "ATTN_STATUS_UNKNOWN";
 }
@@ -341,6 +349,30 @@ attn_status_t mha_layer_fwd(const void* X, const void* W_QKV, const void* W_O, i
     return st;
   // step 5: Y = Concat W_O
   return run_gemm(ds, cat, W_O, Y, static_cast<int>(rows), d_model, d_model, s);
+}
+
+attn_status_t mha_layer_fwd_noalloc(const void* X, const void* W_QKV, const void* W_O, int B,
+                                    int L, int d_model, int h, int mask_kind,
+                                    const int32_t* kv_lens, float scale, void* Y, void* stream) {
+  const size_t need = mha_layer_workspace_bytes(B, L, d_model, h);
+  if (need > ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_TOO_LARGE;
+  DeviceState* ds = nullptr;
+  attn_status_t st = device_state(&ds, nullptr);
+  if (st != ATTN_OK) return st;
+  void* scratch = nullptr;
+  {
+    // once per device, with that device current: the array's device address
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (ds->noalloc_scratch == nullptr) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+        return ATTN_ERR_CUDA;
+      ds->noalloc_scratch = p;
+    }
+    scratch = ds->noalloc_scratch;
+  }
+  return mha_layer_fwd(X, W_QKV, W_O, B, L, d_model, h, mask_kind, kv_lens, scale, Y, scratch,
+                       ATTN_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 attn_status_t attn_check_device_status(void* stream) {
