@@ -16,15 +16,17 @@
 //                    longest-first and dealt to CTAs in a boustrophedon order
 //   warps 0-3      = softmax group for Q tile 0 (rows 0..127 of the block)
 //   warps 4-7      = softmax group for Q tile 1 (rows 128..255)
-//   warp 8         = MMA issuer (one thread) + TMEM owner
+//   warp 8         = MMA issuer of Q tile 0 (one thread) + TMEM owner
 //   warp 9         = TMA producer (one thread)
+//   warp 10        = MMA issuer of Q tile 1 (one thread)
+//   warp 11        = idle (it completes the third warpgroup, which the
+//                    per-warpgroup register reallocation needs)
 // TMEM (512 columns x 128 lanes, fp32):
-//   [  0,128) S of tile 0, its first 64 columns reused for P (bf16 pairs)
+//   [  0,128) S of tile 0; P (bf16 pairs) reuses its high 64 columns
 //   [128,256) S / P of tile 1
 //   [256,384) O accumulator of tile 0, [384,512) O of tile 1
-// Per KV tile j the MMA thread issues S0 = Q0 K_j^T, S1 = Q1 K_j^T, then
-// O0 += P0 V_j, O1 += P1 V_j.  While one softmax group works on its S, the
-// tensor core runs the other group's GEMMs.
+// Each Q tile has its own MMA issuer; while one softmax group works on its
+// S, the tensor core runs the other tile's P.V and next S.
 //
 // Softmax state per row (one thread per row = one TMEM lane): m in log2
 // units (already multiplied by scale*log2 e) and two running sums: l of the
@@ -43,7 +45,13 @@
 
 namespace gb300 {
 
-constexpr int ATTN_THREADS = 320;
+constexpr int ATTN_THREADS = 384;      // 3 warpgroups
+constexpr int ATTN_REGS_AT_LAUNCH = 168;  // 65536 / 384, rounded down to 8
+constexpr int ATTN_REGS_SOFTMAX = 216;
+constexpr int ATTN_REGS_CONTROL = 72;
+static_assert(2 * 128 * ATTN_REGS_SOFTMAX + 128 * ATTN_REGS_CONTROL <=
+                  ATTN_THREADS * ATTN_REGS_AT_LAUNCH,
+              "register split exceeds the registers the block is launched with");
 constexpr int ATTN_BLOCK_M = 128;  // query rows per Q tile
 constexpr int ATTN_BLOCK_N = 128;  // keys per KV tile
 constexpr int ATTN_QTILES = 2;     // Q tiles per work item
@@ -85,12 +93,13 @@ struct AttnLayout {
   static constexpr int B_Q_EMPTY = 2;
   static constexpr int B_K_FULL = 4;
   static constexpr int B_V_FULL = B_K_FULL + STAGES;
-  static constexpr int B_KV_EMPTY = B_V_FULL + STAGES;
-  static constexpr int B_S_FULL = B_KV_EMPTY + STAGES;
+  static constexpr int B_K_EMPTY = B_V_FULL + STAGES;
+  static constexpr int B_V_EMPTY = B_K_EMPTY + STAGES;
+  static constexpr int B_S_FULL = B_V_EMPTY + STAGES;
   static constexpr int B_P_FULL = B_S_FULL + 2;
   static constexpr int B_O_DONE = B_P_FULL + 2;
-  static constexpr int B_DRAIN = B_O_DONE + 2;
-  static constexpr int N_BARS = B_DRAIN + 1;
+  static constexpr int B_DRAIN = B_O_DONE + 2;  // one per MMA issuer
+  static constexpr int N_BARS = B_DRAIN + 2;
   static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
 };
@@ -187,8 +196,10 @@ __device__ __forceinline__ void attn_tma_role(const CUtensorMap* tmQ, const CUte
     }
     for (int j = 0; ok && j < it.nkv_max; ++j, ++kv_it) {
       const int s = static_cast<int>(kv_it % L::STAGES);
+      // a stage's K and V are released separately: K after the last S = Q K^T
+      // that reads it, V after the last P.V
       if (kv_it >= static_cast<uint32_t>(L::STAGES)) {
-        ok = mbar_wait(&bars[L::B_KV_EMPTY + s], ((kv_it / L::STAGES) - 1u) & 1u, ctl);
+        ok = mbar_wait(&bars[L::B_K_EMPTY + s], ((kv_it / L::STAGES) - 1u) & 1u, ctl);
         if (!ok) break;
       }
       if (static_cast<long long>(kv_it) != p.debug_skip_kv_load) {
@@ -196,6 +207,10 @@ __device__ __forceinline__ void attn_tma_role(const CUtensorMap* tmQ, const CUte
         for (int c = 0; c < L::NCHUNK; ++c)
           attn_load_tile(tmK, smem + L::K_OFF + s * L::TILE_BYTES + c * L::CHUNK_BYTES,
                          &bars[L::B_K_FULL + s], 64 * c, j * ATTN_BLOCK_N, it.h, it.b, p.packed);
+      }
+      if (kv_it >= static_cast<uint32_t>(L::STAGES)) {
+        ok = mbar_wait(&bars[L::B_V_EMPTY + s], ((kv_it / L::STAGES) - 1u) & 1u, ctl);
+        if (!ok) break;
       }
       mbar_arrive_expect_tx(&bars[L::B_V_FULL + s], L::TILE_BYTES);
       for (int c = 0; c < L::NCHUNK; ++c)
@@ -219,84 +234,115 @@ __device__ __forceinline__ void attn_tma_role(const CUtensorMap* tmQ, const CUte
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (one thread)
+// MMA issuers: one thread per Q tile
 // ---------------------------------------------------------------------------
+// One tcgen05.mma takes a single issuing thread ~100 cycles, more than the
+// 64-cycle tensor time of a 128 x 128 x 16 step, so each Q tile has its own
+// issuer and the two interleave on the tensor core.
+//
+// Issuer t, per KV tile j:  [wait P_t(j)]  O_t += P_t(j) V_j
+//                           S_t(j+1) = Q_t K_{j+1}^T
+// S_t(j+1) overwrites the TMEM columns that hold P_t(j).  Both MMAs come
+// from the same thread in that order, and the tensor core executes one
+// thread's MMAs in issue order, so P_t(j) has been read before S_t(j+1)
+// writes.  The S_FULL commit after S_t(j+1) fires only when every earlier
+// MMA of the thread, including P_t(j) V_j, has completed, so the softmax may
+// rescale O_t once it sees S_t(j+1).
+//
+// A stage's K and V are released when both issuers have arrived: with a
+// commit after their last MMA that reads it, or with a plain arrive for a KV
+// tile their Q tile does not need (causal tails), after waiting for the tile
+// to land so that an arrival can never count towards an earlier use of the
+// stage.
 template <int D>
-__device__ __forceinline__ void attn_mma_role(const AttnParams& p, uint8_t* smem, uint64_t* bars,
-                                              uint32_t tmem, const WaitCtl& ctl) {
+__device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, uint8_t* smem,
+                                              uint64_t* bars, uint32_t tmem, const WaitCtl& ctl) {
   using L = AttnLayout<D>;
   constexpr uint32_t IDESC_S = idesc_bf16_f32(ATTN_BLOCK_M, ATTN_BLOCK_N, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(ATTN_BLOCK_M, D, true);
-  const uint32_t q_base = smem_u32(smem + L::Q_OFF);
+  const uint32_t qa = smem_u32(smem + L::Q_OFF) + t * L::TILE_BYTES;
   const uint32_t k_base = smem_u32(smem + L::K_OFF);
   const uint32_t v_base = smem_u32(smem + L::V_OFF);
-  uint32_t q_uses[ATTN_QTILES] = {0u, 0u};
-  uint32_t p_cnt[ATTN_QTILES] = {0u, 0u};
-  uint32_t pv_cnt[ATTN_QTILES] = {0u, 0u};
-  uint32_t kv_it = 0;
+  const uint32_t s_tmem = tmem + static_cast<uint32_t>(t * ATTN_BLOCK_N);
+  const uint32_t p_tmem = s_tmem + 64u;  // P in the high half of the S columns
+  const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(t * 128);
+  uint32_t q_uses = 0, p_cnt = 0;
+  uint32_t kv_it = 0;  // running KV tile index (stage = kv_it % STAGES)
   bool ok = true;
   AttnItem it;
   for (int k = 0; ok && attn_get_item(p, k, it); ++k) {
-    if (it.kv_len_raw != it.kv_len) atomicOr(p.status, ATTN_STATUS_BAD_KVLEN);
+    if (t == 0 && it.kv_len_raw != it.kv_len) atomicOr(p.status, ATTN_STATUS_BAD_KVLEN);
+    if (it.nkv_max == 0) continue;
+    const int nkv = t ? it.nkv[1] : it.nkv[0];
+    // S_t(0)
+    {
+      const int s = static_cast<int>(kv_it % L::STAGES);
+      ok = mbar_wait(&bars[L::B_K_FULL + s], (kv_it / L::STAGES) & 1u, ctl);
+      if (ok && nkv > 0) {
+        ok = mbar_wait(&bars[L::B_Q_FULL + t], q_uses & 1u, ctl);
+        ++q_uses;
+        if (ok) {
+          tc_fence_after();
+          const uint32_t ka = k_base + s * L::TILE_BYTES;
 #pragma unroll
-    for (int t = 0; t < ATTN_QTILES; ++t) {
-      if (ok && it.nkv[t] > 0) {
-        ok = mbar_wait(&bars[L::B_Q_FULL + t], q_uses[t] & 1u, ctl);
-        ++q_uses[t];
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * L::CHUNK_BYTES + (kk & 3) * 32;
+            mma_bf16_ss(s_tmem, smem_desc_sw128(qa + off, 16, 1024),
+                        smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars[L::B_S_FULL + t]);
+          if (nkv == 1) mma_commit(&bars[L::B_Q_EMPTY + t]);
+          mma_commit(&bars[L::B_K_EMPTY + s]);
+        }
+      } else if (ok) {
+        mbar_arrive(&bars[L::B_K_EMPTY + s]);
       }
     }
     for (int j = 0; ok && j < it.nkv_max; ++j, ++kv_it) {
       const int s = static_cast<int>(kv_it % L::STAGES);
-      const uint32_t ph = (kv_it / L::STAGES) & 1u;
-      ok = mbar_wait(&bars[L::B_K_FULL + s], ph, ctl);
-      // S_t = Q_t K_j^T for both Q tiles
-#pragma unroll
-      for (int t = 0; t < ATTN_QTILES; ++t) {
-        if (!ok || j >= it.nkv[t]) continue;
-        // S_t's columns still hold P_t of the previous tile until that P.V is done
-        if (pv_cnt[t] > 0) ok = mbar_wait(&bars[L::B_O_DONE + t], (pv_cnt[t] - 1u) & 1u, ctl);
-        if (!ok) continue;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(t * ATTN_BLOCK_N);
-        const uint32_t qa = q_base + t * L::TILE_BYTES;
-        const uint32_t ka = k_base + s * L::TILE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::CHUNK_BYTES + (kk & 3) * 32;
-          mma_bf16_ss(d_tmem, smem_desc_sw128(qa + off, 16, 1024),
-                      smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars[L::B_S_FULL + t]);
-        if (j == it.nkv[t] - 1) mma_commit(&bars[L::B_Q_EMPTY + t]);
-      }
+      ok = mbar_wait(&bars[L::B_V_FULL + s], (kv_it / L::STAGES) & 1u, ctl);
       if (!ok) break;
-      ok = mbar_wait(&bars[L::B_V_FULL + s], ph, ctl);
-      // O_t += P_t V_j
-#pragma unroll
-      for (int t = 0; t < ATTN_QTILES; ++t) {
-        if (!ok || j >= it.nkv[t]) continue;
-        ok = mbar_wait(&bars[L::B_P_FULL + t], p_cnt[t] & 1u, ctl);
-        if (!ok) continue;
-        ++p_cnt[t];
+      if (j < nkv) {
+        // O_t += P_t(j) V_j
+        ok = mbar_wait(&bars[L::B_P_FULL + t], p_cnt & 1u, ctl);
+        if (!ok) break;
+        ++p_cnt;
         tc_fence_after();
-        const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(t * 128);
-        const uint32_t p_tmem = tmem + static_cast<uint32_t>(t * ATTN_BLOCK_N);
         const uint32_t va = v_base + s * L::TILE_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < ATTN_BLOCK_N / 16; ++kk) {
+        for (int kk = 0; kk < ATTN_BLOCK_N / 16; ++kk)
           mma_bf16_ts(o_tmem, p_tmem + kk * 8, smem_desc_sw128(va + kk * 2048, L::CHUNK_BYTES, 1024),
                       IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
-        }
         mma_commit(&bars[L::B_O_DONE + t]);
-        ++pv_cnt[t];
+        mma_commit(&bars[L::B_V_EMPTY + s]);
+      } else {
+        mbar_arrive(&bars[L::B_V_EMPTY + s]);
       }
-      if (!ok) break;
-      mma_commit(&bars[L::B_KV_EMPTY + s]);
+      if (j + 1 < it.nkv_max) {
+        const int s1 = static_cast<int>((kv_it + 1) % L::STAGES);
+        ok = mbar_wait(&bars[L::B_K_FULL + s1], ((kv_it + 1) / L::STAGES) & 1u, ctl);
+        if (!ok) break;
+        if (j + 1 < nkv) {
+          // S_t(j+1) = Q_t K_{j+1}^T
+          const uint32_t ka = k_base + s1 * L::TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * L::CHUNK_BYTES + (kk & 3) * 32;
+            mma_bf16_ss(s_tmem, smem_desc_sw128(qa + off, 16, 1024),
+                        smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars[L::B_S_FULL + t]);
+          if (j + 2 == nkv) mma_commit(&bars[L::B_Q_EMPTY + t]);
+          mma_commit(&bars[L::B_K_EMPTY + s1]);
+        } else {
+          mbar_arrive(&bars[L::B_K_EMPTY + s1]);
+        }
+      }
     }
   }
   // Unwind: all MMAs issued by this thread complete before TMEM is freed.
-  mma_commit(&bars[L::B_DRAIN]);
-  mbar_wait_drain(&bars[L::B_DRAIN], 0u, ctl.limit_ns);
+  mma_commit(&bars[L::B_DRAIN + t]);
+  mbar_wait_drain(&bars[L::B_DRAIN + t], 0u, ctl.limit_ns);
 }
 
 // ---------------------------------------------------------------------------
@@ -310,6 +356,7 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
   const int rloc = static_cast<int>(threadIdx.x & 127u);
   const uint32_t lane_base = static_cast<uint32_t>(threadIdx.x & 96u) << 16;
   const uint32_t s_tmem = tmem + static_cast<uint32_t>(t * ATTN_BLOCK_N) + lane_base;
+  const uint32_t p_tmem = s_tmem + 64u;  // P in the high half of the S columns
   const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(t * 128) + lane_base;
   const float c = p.scale_log2;
   const bool causal = (p.mask_kind & ATTN_MASK_CAUSAL_BIT) != 0;
@@ -356,29 +403,36 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
         for (int i = 0; i < 128; ++i) s[i] = (i < nvalid) ? s[i] : -INFINITY;
       }
       float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
+      float mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-      for (int i = 4; i < 128; i += 4) {
+      for (int i = 8; i < 128; i += 8) {
         mx0 = fmax3(mx0, s[i], s[i + 1]);
         mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
+        mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
+        mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
       }
-      const float mx = fmaxf(mx0, mx1);
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       const float m_tile = mx * c;  // scale > 0, so the max commutes with it
       const float m_new = fmaxf(m, m_tile);
       const bool need = m_new > m + ATTN_RESCALE_THRESHOLD;
       if (__any_sync(0xffffffffu, need && j > 0)) {
-        // rescale this row's O accumulator; the previous P.V must be done
-        ok = mbar_wait(&bars[L::B_O_DONE + t], (pv_cnt - 1u) & 1u, ctl);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
+        // rescale this row's O accumulator.  P_t(j-1) V has completed: the
+        // commit that signalled S_t(j) covers every earlier MMA of the issuer.
         const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
+        const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t ro[32];
           tmem_ld_32x32b_x32(o_tmem + cc * 32u, ro);
           tmem_ld_wait(ro);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(ro[2 * i]), __uint_as_float(ro[2 * i + 1])), a2),
+                      x0, x1);
+            ro[2 * i] = __float_as_uint(x0);
+            ro[2 * i + 1] = __float_as_uint(x1);
+          }
           tmem_st_32x32b_x32(o_tmem + cc * 32u, ro);
         }
         tmem_st_wait();
@@ -390,41 +444,48 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
         m = m_new;
       }
       const float mb = (m == -INFINITY) ? 0.f : m;
-      // p = 2^(s*c - m); P goes to TMEM as bf16 pairs.  Two row sums: lf of
+      // p = 2^(s*c - m); P goes to TMEM as bf16 pairs.  Two row sums: l of
       // the fp32 p (for the LSE) and lb of the bf16-rounded p that the tensor
       // core multiplies into V (for the normalisation of O).
       const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-mb, -mb);
-      uint64_t lf2 = 0ull, lb2 = 0ull;
+      uint64_t lf_a = 0ull, lf_b = 0ull;
+      float lb_a = 0.f, lb_b = 0.f, lb_c = 0.f, lb_d = 0.f;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float a0, a1;
+        for (int i = 0; i < 32; i += 2) {
+          float a0, a1, a2, a3;
           f2_unpack(f2_fma(f2_pack(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]), c2, nm2), a0,
                     a1);
-          const float p0 = ex2_approx(a0);
-          const float p1 = ex2_approx(a1);
+          f2_unpack(f2_fma(f2_pack(s[64 * half + 2 * i + 2], s[64 * half + 2 * i + 3]), c2, nm2),
+                    a2, a3);
+          const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+          const float p2 = ex2_approx(a2), p3 = ex2_approx(a3);
           pk[i] = pack_bf16x2(p0, p1);
-          lf2 = f2_add(lf2, f2_pack(p0, p1));
-          lb2 = f2_add(lb2, f2_pack(bf16x2_lo(pk[i]), bf16x2_hi(pk[i])));
+          pk[i + 1] = pack_bf16x2(p2, p3);
+          lf_a = f2_add(lf_a, f2_pack(p0, p1));
+          lf_b = f2_add(lf_b, f2_pack(p2, p3));
+          lb_a = add_bf16lo_f32(lb_a, pk[i]);
+          lb_b = add_bf16hi_f32(lb_b, pk[i]);
+          lb_c = add_bf16lo_f32(lb_c, pk[i + 1]);
+          lb_d = add_bf16hi_f32(lb_d, pk[i + 1]);
         }
-        tmem_st_32x32b_x32(s_tmem + 32u * half, pk);
-        tmem_st_wait();
+        tmem_st_32x32b_x32(p_tmem + 32u * half, pk);
       }
       {
-        float x0, x1, y0, y1;
-        f2_unpack(lf2, x0, x1);
-        f2_unpack(lb2, y0, y1);
+        float x0, x1;
+        f2_unpack(f2_add(lf_a, lf_b), x0, x1);
         l += x0 + x1;
-        lb += y0 + y1;
+        lb += (lb_a + lb_b) + (lb_c + lb_d);
       }
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars[L::B_P_FULL + t]);
       ++pv_cnt;
     }
     if (!ok) break;
-    // epilogue: O / l (bf16), LSE; padded and empty rows are exactly 0 / -inf
+    // epilogue: O / lb (bf16), LSE; padded and empty rows are exactly 0 / -inf
     if (nkv > 0) {
       ok = mbar_wait(&bars[L::B_O_DONE + t], (pv_cnt - 1u) & 1u, ctl);
       ok = __all_sync(0xffffffffu, ok);
@@ -495,9 +556,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(&bars[L::B_K_FULL + s], 1);
       mbar_init(&bars[L::B_V_FULL + s], 1);
-      mbar_init(&bars[L::B_KV_EMPTY + s], 1);
+      mbar_init(&bars[L::B_K_EMPTY + s], ATTN_QTILES);  // one arrival per MMA issuer
+      mbar_init(&bars[L::B_V_EMPTY + s], ATTN_QTILES);
     }
-    mbar_init(&bars[L::B_DRAIN], 1);
+    mbar_init(&bars[L::B_DRAIN + 0], 1);
+    mbar_init(&bars[L::B_DRAIN + 1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -511,12 +574,20 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns, ATTN_STATUS_TIMEOUT};
 
-  if (warp == 9) {
-    if (lane == 0) attn_tma_role<D>(&tmQ, &tmK, &tmV, p, smem, bars, ctl);
-  } else if (warp == 8) {
-    if (lane == 0) attn_mma_role<D>(p, smem, bars, tmem, ctl);
-    __syncwarp();
+  // Register split: the two softmax warpgroups take 216 registers per
+  // thread, the control warpgroup (MMA, TMA and two idle warps) 72; together
+  // exactly the 384 x 168 registers the block is launched with (the host
+  // refuses to launch a build whose launch register count differs).
+  if (warp >= 8) {
+    reg_dealloc<ATTN_REGS_CONTROL>();
+    if (warp == 9) {
+      if (lane == 0) attn_tma_role<D>(&tmQ, &tmK, &tmV, p, smem, bars, ctl);
+    } else if (warp == 8 || warp == 10) {
+      if (lane == 0) attn_mma_role<D>(warp == 8 ? 0 : 1, p, smem, bars, tmem, ctl);
+      __syncwarp();
+    }
   } else {
+    reg_alloc<ATTN_REGS_SOFTMAX>();
     attn_softmax_role<D>(warp >> 2, p, bars, tmem, ctl);
   }
 

@@ -124,6 +124,13 @@ attn_status_t launch_attn(DeviceState* ds, int attr_idx, const CUtensorMap& mq,
                           cudaStream_t stream) {
   using L = gb300::AttnLayout<D>;
   if (!ds->attn_attr[attr_idx]) {
+    // The kernel hands registers between warpgroups (setmaxnreg); the split
+    // adds up to exactly ATTN_THREADS x ATTN_REGS_AT_LAUNCH, so a build with a
+    // different launch register count could wait forever: refuse it.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, gb300::attn_fwd_kernel<D>) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (fa.numRegs != gb300::ATTN_REGS_AT_LAUNCH || fa.maxThreadsPerBlock < gb300::ATTN_THREADS)
+      return ATTN_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(gb300::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::SMEM_BYTES) != cudaSuccess)
       return ATTN_ERR_CUDA;

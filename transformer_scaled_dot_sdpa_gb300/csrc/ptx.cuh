@@ -312,6 +312,34 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// acc + (one bf16 half of a packed pair), in fp32 (sm_100+ mixed precision)
+__device__ __forceinline__ float add_bf16lo_f32(float acc, uint32_t pk) {
+  float d;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "add.rn.f32.bf16 %0, lo, %2;\n\t}"
+      : "=f"(d)
+      : "r"(pk), "f"(acc));
+  return d;
+}
+__device__ __forceinline__ float add_bf16hi_f32(float acc, uint32_t pk) {
+  float d;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "add.rn.f32.bf16 %0, hi, %2;\n\t}"
+      : "=f"(d)
+      : "r"(pk), "f"(acc));
+  return d;
+}
+
+// Per-warpgroup register reallocation (every warp of the warpgroup executes it).
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // The two bf16 halves of a packed pair, widened to float (exact).
 __device__ __forceinline__ float bf16x2_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16x2_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
