@@ -93,9 +93,8 @@ struct AttnLayout {
   static constexpr int B_Q_EMPTY = 2;
   static constexpr int B_K_FULL = 4;
   static constexpr int B_V_FULL = B_K_FULL + STAGES;
-  static constexpr int B_K_EMPTY = B_V_FULL + STAGES;
-  static constexpr int B_V_EMPTY = B_K_EMPTY + STAGES;
-  static constexpr int B_S_FULL = B_V_EMPTY + STAGES;
+  static constexpr int B_KV_EMPTY = B_V_FULL + STAGES;
+  static constexpr int B_S_FULL = B_KV_EMPTY + STAGES;
   static constexpr int B_P_FULL = B_S_FULL + 2;
   static constexpr int B_O_DONE = B_P_FULL + 2;
   static constexpr int B_DRAIN = B_O_DONE + 2;  // one per MMA issuer
@@ -196,10 +195,9 @@ __device__ __forceinline__ void attn_tma_role(const CUtensorMap* tmQ, const CUte
     }
     for (int j = 0; ok && j < it.nkv_max; ++j, ++kv_it) {
       const int s = static_cast<int>(kv_it % L::STAGES);
-      // a stage's K and V are released separately: K after the last S = Q K^T
-      // that reads it, V after the last P.V
+      // a stage is free once both MMA issuers released it
       if (kv_it >= static_cast<uint32_t>(L::STAGES)) {
-        ok = mbar_wait(&bars[L::B_K_EMPTY + s], ((kv_it / L::STAGES) - 1u) & 1u, ctl);
+        ok = mbar_wait(&bars[L::B_KV_EMPTY + s], ((kv_it / L::STAGES) - 1u) & 1u, ctl);
         if (!ok) break;
       }
       if (static_cast<long long>(kv_it) != p.debug_skip_kv_load) {
@@ -207,10 +205,6 @@ __device__ __forceinline__ void attn_tma_role(const CUtensorMap* tmQ, const CUte
         for (int c = 0; c < L::NCHUNK; ++c)
           attn_load_tile(tmK, smem + L::K_OFF + s * L::TILE_BYTES + c * L::CHUNK_BYTES,
                          &bars[L::B_K_FULL + s], 64 * c, j * ATTN_BLOCK_N, it.h, it.b, p.packed);
-      }
-      if (kv_it >= static_cast<uint32_t>(L::STAGES)) {
-        ok = mbar_wait(&bars[L::B_V_EMPTY + s], ((kv_it / L::STAGES) - 1u) & 1u, ctl);
-        if (!ok) break;
       }
       mbar_arrive_expect_tx(&bars[L::B_V_FULL + s], L::TILE_BYTES);
       for (int c = 0; c < L::NCHUNK; ++c)
@@ -249,14 +243,31 @@ __device__ __forceinline__ void attn_tma_role(const CUtensorMap* tmQ, const CUte
 // MMA of the thread, including P_t(j) V_j, has completed, so the softmax may
 // rescale O_t once it sees S_t(j+1).
 //
-// A stage's K and V are released when both issuers have arrived: with a
-// commit after their last MMA that reads it, or with a plain arrive for a KV
-// tile their Q tile does not need (causal tails), after waiting for the tile
-// to land so that an arrival can never count towards an earlier use of the
-// stage.
+// A K/V stage is released when both issuers have arrived: with a commit
+// after their P.V of that KV tile (which follows the S that read its K), or
+// with a plain arrive for a KV tile their Q tile does not need (causal
+// tails), after waiting for the tile to land so that an arrival can never
+// count towards an earlier use of the stage.  O_DONE is signalled only after
+// an item's last P.V, for the epilogue.
+// Bounded poll of a shared flag (set once, never cleared).
+__device__ __forceinline__ bool attn_wait_flag(volatile int* flag, const WaitCtl& c) {
+  const uint64_t t0 = globaltimer_ns();
+  while (*flag == 0) {
+    if (*c.abort_flag) return false;
+    if (globaltimer_ns() - t0 > c.limit_ns) {
+      *c.abort_flag = 1;
+      atomicOr(c.status, c.timeout_code);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
 template <int D>
 __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, uint8_t* smem,
-                                              uint64_t* bars, uint32_t tmem, const WaitCtl& ctl) {
+                                              uint64_t* bars, uint32_t tmem, const WaitCtl& ctl,
+                                              volatile int* tile0_started) {
   using L = AttnLayout<D>;
   constexpr uint32_t IDESC_S = idesc_bf16_f32(ATTN_BLOCK_M, ATTN_BLOCK_N, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(ATTN_BLOCK_M, D, true);
@@ -274,8 +285,12 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
     if (t == 0 && it.kv_len_raw != it.kv_len) atomicOr(p.status, ATTN_STATUS_BAD_KVLEN);
     if (it.nkv_max == 0) continue;
     const int nkv = t ? it.nkv[1] : it.nkv[0];
+    // The two Q tiles' chains (S -> softmax -> P.V) are independent; tile 1
+    // starts half a chain late so that the two softmax groups alternate on
+    // the SM instead of competing.
+    if (t == 1 && k == 0 && it.nkv[0] > 0 && nkv > 0) ok = attn_wait_flag(tile0_started, ctl);
     // S_t(0)
-    {
+    if (ok) {
       const int s = static_cast<int>(kv_it % L::STAGES);
       ok = mbar_wait(&bars[L::B_K_FULL + s], (kv_it / L::STAGES) & 1u, ctl);
       if (ok && nkv > 0) {
@@ -292,10 +307,7 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
           }
           mma_commit(&bars[L::B_S_FULL + t]);
           if (nkv == 1) mma_commit(&bars[L::B_Q_EMPTY + t]);
-          mma_commit(&bars[L::B_K_EMPTY + s]);
         }
-      } else if (ok) {
-        mbar_arrive(&bars[L::B_K_EMPTY + s]);
       }
     }
     for (int j = 0; ok && j < it.nkv_max; ++j, ++kv_it) {
@@ -313,10 +325,12 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
         for (int kk = 0; kk < ATTN_BLOCK_N / 16; ++kk)
           mma_bf16_ts(o_tmem, p_tmem + kk * 8, smem_desc_sw128(va + kk * 2048, L::CHUNK_BYTES, 1024),
                       IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars[L::B_O_DONE + t]);
-        mma_commit(&bars[L::B_V_EMPTY + s]);
+        // K_j (read by S_t(j), issued earlier) and V_j are free once this
+        // P.V completes; O_t is final after the item's last P.V
+        mma_commit(&bars[L::B_KV_EMPTY + s]);
+        if (j == nkv - 1) mma_commit(&bars[L::B_O_DONE + t]);
       } else {
-        mbar_arrive(&bars[L::B_V_EMPTY + s]);
+        mbar_arrive(&bars[L::B_KV_EMPTY + s]);
       }
       if (j + 1 < it.nkv_max) {
         const int s1 = static_cast<int>((kv_it + 1) % L::STAGES);
@@ -333,9 +347,6 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
           }
           mma_commit(&bars[L::B_S_FULL + t]);
           if (j + 2 == nkv) mma_commit(&bars[L::B_Q_EMPTY + t]);
-          mma_commit(&bars[L::B_K_EMPTY + s1]);
-        } else {
-          mbar_arrive(&bars[L::B_K_EMPTY + s1]);
         }
       }
     }
@@ -351,7 +362,7 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
 template <int D>
 __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams& p,
                                                   uint64_t* bars, uint32_t tmem,
-                                                  const WaitCtl& ctl) {
+                                                  const WaitCtl& ctl, volatile int* tile0_started) {
   using L = AttnLayout<D>;
   const int rloc = static_cast<int>(threadIdx.x & 127u);
   const uint32_t lane_base = static_cast<uint32_t>(threadIdx.x & 96u) << 16;
@@ -361,7 +372,7 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
   const float c = p.scale_log2;
   const bool causal = (p.mask_kind & ATTN_MASK_CAUSAL_BIT) != 0;
   const bool padding = (p.mask_kind & ATTN_MASK_PADDING_BIT) != 0;
-  uint32_t s_cnt = 0, pv_cnt = 0;
+  uint32_t s_cnt = 0, o_cnt = 0;  // completions seen of S_FULL[t], O_DONE[t]
   bool ok = true;
   AttnItem it;
   for (int k = 0; ok && attn_get_item(p, k, it); ++k) {
@@ -482,12 +493,13 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars[L::B_P_FULL + t]);
-      ++pv_cnt;
+      if (t == 0 && k == 0 && j == 0 && threadIdx.x == 0) *tile0_started = 1;
     }
     if (!ok) break;
     // epilogue: O / lb (bf16), LSE; padded and empty rows are exactly 0 / -inf
     if (nkv > 0) {
-      ok = mbar_wait(&bars[L::B_O_DONE + t], (pv_cnt - 1u) & 1u, ctl);
+      ok = mbar_wait(&bars[L::B_O_DONE + t], o_cnt & 1u, ctl);
+      ++o_cnt;
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -542,10 +554,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+  volatile int* tile0_started = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 8);
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31u);
 
   if (threadIdx.x == 0) {
+    *tile0_started = 0;
     for (int t = 0; t < ATTN_QTILES; ++t) {
       mbar_init(&bars[L::B_Q_FULL + t], 1);
       mbar_init(&bars[L::B_Q_EMPTY + t], 1);
@@ -556,8 +570,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(&bars[L::B_K_FULL + s], 1);
       mbar_init(&bars[L::B_V_FULL + s], 1);
-      mbar_init(&bars[L::B_K_EMPTY + s], ATTN_QTILES);  // one arrival per MMA issuer
-      mbar_init(&bars[L::B_V_EMPTY + s], ATTN_QTILES);
+      mbar_init(&bars[L::B_KV_EMPTY + s], ATTN_QTILES);  // one arrival per MMA issuer
     }
     mbar_init(&bars[L::B_DRAIN + 0], 1);
     mbar_init(&bars[L::B_DRAIN + 1], 1);
@@ -583,12 +596,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     if (warp == 9) {
       if (lane == 0) attn_tma_role<D>(&tmQ, &tmK, &tmV, p, smem, bars, ctl);
     } else if (warp == 8 || warp == 10) {
-      if (lane == 0) attn_mma_role<D>(warp == 8 ? 0 : 1, p, smem, bars, tmem, ctl);
+      if (lane == 0) attn_mma_role<D>(warp == 8 ? 0 : 1, p, smem, bars, tmem, ctl, tile0_started);
       __syncwarp();
     }
   } else {
     reg_alloc<ATTN_REGS_SOFTMAX>();
-    attn_softmax_role<D>(warp >> 2, p, bars, tmem, ctl);
+    attn_softmax_role<D>(warp >> 2, p, bars, tmem, ctl, tile0_started);
   }
 
   tc_fence_before();
