@@ -138,14 +138,23 @@ def dist_env():
     return world, rank, local
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
+    """Max of a per-rank scalar over all ranks (the slowest rank's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_workload(w, rank):
+    """Rank r's replica: the same shapes, an independent seed (weak scaling;
+    attention of distinct sequences needs no exchange between ranks)."""
+    if rank == 0:
+        return w
+    return type(w)(**{**w.__dict__, "seed": w.seed + 7919 * rank})
 
 
 def barrier(world):
@@ -241,9 +250,7 @@ def ours_arm(args, w):
     torch.cuda.set_device(dev)
     import transformer_scaled_dot_sdpa_gb300 as g
 
-    # replicas draw distinct data (independent problems)
-    w_rank = w if rank == 0 else type(w)(**{**w.__dict__, "seed": w.seed + 7919 * rank})
-    inp = make_workload_inputs(w_rank)
+    inp = make_workload_inputs(replica_workload(w, rank))
     kv_lens = inp["kv_lens"]
 
     def pinned(bits):
