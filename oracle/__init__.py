@@ -11,8 +11,9 @@ Functions
 ---------
 attention(q, k, v, mask_kind=0, kv_lens=None, scale=None, rows=None,
           want_weights=False, nthreads=None) -> (O, LSE[, A])
-    Q [B,H,Lq,dk], K [B,H,Lk,dk], V [B,H,Lk,dv]: uint16 bfloat16 bit patterns
-    or float64.  Definition: "04. Self-Attention：Transformer 的核心计算",
+    Q [B,H,Lq,dk], K [B,Hkv,Lk,dk], V [B,Hkv,Lk,dv] (Hkv divides H: grouped-
+    query attention, "Self-Attention 机制", section MHA -> MQA -> GQA -> MLA):
+    uint16 bfloat16 bit patterns or float64.  Definition: "04. Self-Attention：Transformer 的核心计算",
     sections 四 and 七; "attention-mechanism" page, sections on the sqrt(d_k)
     scale and on causal / padding masks.
 mha_layer(x, w_qkv, w_o, H, mask_kind=0, kv_lens=None, scale=None, rows=None,
@@ -37,6 +38,7 @@ _lib = None
 MASK_NONE = 0
 MASK_CAUSAL = 1
 MASK_PADDING = 2
+MASK_CAUSAL_BOTTOM_RIGHT = 4
 
 
 def build(force: bool = False) -> str:
@@ -55,8 +57,8 @@ class OracleLib:
         lib = ctypes.CDLL(path)
         vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
         lib.oracle_attention.restype = i32
-        lib.oracle_attention.argtypes = [i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp,
-                                         dbl, vp, i64, vp, vp, vp, i32]
+        lib.oracle_attention.argtypes = [i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
+                                         vp, dbl, vp, i64, vp, vp, vp, i32]
         lib.oracle_mha_layer.restype = i32
         lib.oracle_mha_layer.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, dbl, vp, i64,
                                          vp, i32]
@@ -130,9 +132,9 @@ def _attention(lib, q, k, v, mask_kind=MASK_NONE, kv_lens=None, scale=None, rows
     if not (qb == kb == vb):
         raise TypeError("q, k, v must share one element type")
     B, H, Lq, dk = q.shape
-    Lk = k.shape[2]
+    Hkv, Lk = k.shape[1], k.shape[2]
     dv = v.shape[3]
-    if k.shape != (B, H, Lk, dk) or v.shape != (B, H, Lk, dv):
+    if k.shape != (B, Hkv, Lk, dk) or v.shape != (B, Hkv, Lk, dv) or H % Hkv != 0:
         raise ValueError("shape mismatch")
     kl = None
     if mask_kind & MASK_PADDING:
@@ -145,7 +147,8 @@ def _attention(lib, q, k, v, mask_kind=MASK_NONE, kv_lens=None, scale=None, rows
     O = np.empty((n, dv), dtype=np.float64)
     LSE = np.empty((n,), dtype=np.float64)
     A = np.empty((n, Lk), dtype=np.float64) if want_weights else None
-    rc = lib.oracle_attention(qb, _ptr(q), _ptr(k), _ptr(v), B, H, Lq, Lk, dk, dv, int(mask_kind),
+    rc = lib.oracle_attention(qb, _ptr(q), _ptr(k), _ptr(v), B, H, Hkv, Lq, Lk, dk, dv,
+                              int(mask_kind),
                               _ptr(kl), float(scale) if scale else 0.0, _ptr(rr),
                               n, _ptr(O), _ptr(LSE), _ptr(A),
                               int(nthreads or default_threads()))

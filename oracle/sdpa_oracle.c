@@ -18,6 +18,7 @@
  *
  *   For each (b, head, query row i), in fp64:
  *     J_i  = { j < Lk }  intersected with { j <= i } if CAUSAL
+ *                        intersected with { j <= i + Lk - Lq } if CAUSAL_BR
  *                        intersected with { j < kv_len[b] } if PADDING
  *     s_j  = scale * sum_c Q[i,c] K[j,c]          for j in J_i
  *     m    = max_j s_j                            (max subtraction, the
@@ -30,6 +31,17 @@
  *     LSE[i] = m + log(l)
  *   A padded query row (PADDING and i >= kv_len[b]) or a row whose J_i is
  *   empty has O[i] = 0 and LSE[i] = -inf.
+ *
+ *   Grouped-query attention ("Self-Attention 机制", section
+ *   "MHA -> MQA -> GQA -> MLA"): with H query heads and Hkv key/value heads
+ *   (H a multiple of Hkv), each run of H/Hkv consecutive query heads shares one
+ *   K/V head: query head h reads K/V head h / (H/Hkv).  Hkv = H is ordinary
+ *   multi-head attention, Hkv = 1 multi-query attention.
+ *
+ *   CAUSAL_BR is the causal mask aligned to the last key instead of the first
+ *   (query i sits at key position i + Lk - Lq), the reading used when Lq
+ *   queries continue a sequence whose Lk keys include them; for Lq = Lk it is
+ *   the ordinary causal mask.
  *
  *   The multi-head layer ("Self-Attention 机制", section "五步计算" and the
  *   shape trace in "维度全程跟踪"; "多模态大模型学习笔记（十四）", section 3.3):
@@ -53,6 +65,7 @@
 
 #define OR_MASK_CAUSAL 1
 #define OR_MASK_PADDING 2
+#define OR_MASK_CAUSAL_BR 4
 
 #define OR_OK 0
 #define OR_ERR_ARG (-1)
@@ -126,11 +139,17 @@ static void attend_row(const double *q, const double *K, size_t k_stride,
 }
 
 /* Number of keys row i of batch b may attend to (J_i is always a prefix). */
-static int valid_keys(int i, int Lk, int mask_kind, int kv_len)
+static int valid_keys(int i, int Lq, int Lk, int mask_kind, int kv_len)
 {
     int n = Lk;
     if (mask_kind & OR_MASK_CAUSAL)
         n = (i + 1 < n) ? i + 1 : n;
+    if (mask_kind & OR_MASK_CAUSAL_BR) {
+        long long lim = (long long)i + 1 + (long long)Lk - (long long)Lq;
+        if (lim < 0)
+            lim = 0;
+        n = (lim < n) ? (int)lim : n;
+    }
     if (mask_kind & OR_MASK_PADDING) {
         if (i >= kv_len)
             return 0; /* padded query row: output 0 */
@@ -145,7 +164,7 @@ static int valid_keys(int i, int Lk, int mask_kind, int kv_len)
 typedef struct {
     int is_bf16;
     const void *Q, *K, *V;
-    int B, H, Lq, Lk, dk, dv, mask_kind;
+    int B, H, Hkv, Lq, Lk, dk, dv, mask_kind;
     const int32_t *kv_lens;
     double scale;
     const int64_t *rows; /* flat (b*H + h)*Lq + i, sorted by head, or NULL */
@@ -177,7 +196,7 @@ static void *attn_worker(void *arg)
     }
     for (;;) {
         int64_t u = __atomic_fetch_add(&J->next_unit, 1, __ATOMIC_RELAXED);
-        int64_t r0, r1, r, bh;
+        int64_t r0, r1, r, bh, kvbh;
         int b, max_keys, kv_len, j, c;
         if (u >= J->n_units)
             break;
@@ -185,12 +204,14 @@ static void *attn_worker(void *arg)
         r1 = J->unit_start[u + 1];
         bh = row_id(J, r0) / J->Lq;
         b = (int)(bh / J->H);
+        /* the K/V head this query head reads (grouped-query attention) */
+        kvbh = (int64_t)b * J->Hkv + (int)(bh % J->H) / (J->H / J->Hkv);
         kv_len = (J->mask_kind & OR_MASK_PADDING) ? J->kv_lens[b] : J->Lk;
         /* widen the keys/values this block of rows needs */
         max_keys = 0;
         for (r = r0; r < r1; ++r) {
             int i = (int)(row_id(J, r) % J->Lq);
-            int n = valid_keys(i, J->Lk, J->mask_kind, kv_len);
+            int n = valid_keys(i, J->Lq, J->Lk, J->mask_kind, kv_len);
             if (n > max_keys)
                 max_keys = n;
         }
@@ -206,8 +227,8 @@ static void *attn_worker(void *arg)
             }
         }
         for (j = 0; j < max_keys; ++j) {
-            size_t kb = ((size_t)bh * (size_t)J->Lk + (size_t)j) * (size_t)J->dk;
-            size_t vb = ((size_t)bh * (size_t)J->Lk + (size_t)j) * (size_t)J->dv;
+            size_t kb = ((size_t)kvbh * (size_t)J->Lk + (size_t)j) * (size_t)J->dk;
+            size_t vb = ((size_t)kvbh * (size_t)J->Lk + (size_t)j) * (size_t)J->dv;
             for (c = 0; c < J->dk; ++c)
                 Kd[(size_t)j * J->dk + c] = elem(J->K, J->is_bf16, kb + c);
             for (c = 0; c < J->dv; ++c)
@@ -216,7 +237,7 @@ static void *attn_worker(void *arg)
         for (r = r0; r < r1; ++r) {
             int64_t id = row_id(J, r);
             int i = (int)(id % J->Lq);
-            int n = valid_keys(i, J->Lk, J->mask_kind, kv_len);
+            int n = valid_keys(i, J->Lq, J->Lk, J->mask_kind, kv_len);
             size_t qb = (size_t)id * (size_t)J->dk;
             double *a_row = J->A ? J->A + (size_t)r * (size_t)J->Lk : NULL;
             for (c = 0; c < J->dk; ++c)
@@ -260,7 +281,7 @@ static int run_threads(void *(*fn)(void *), void *job, int nthreads)
 /*
  * oracle_attention: see the file header for the definition.
  *   elem_is_bf16: 1 -> Q/K/V are uint16 bf16 bit patterns, 0 -> fp64.
- *   Q [B,H,Lq,dk], K [B,H,Lk,dk], V [B,H,Lk,dv], contiguous.
+ *   Q [B,H,Lq,dk], K [B,Hkv,Lk,dk], V [B,Hkv,Lk,dv], contiguous; H % Hkv == 0.
  *   kv_lens: int32 [B], required when the PADDING bit is set; each in [0, Lk].
  *   scale <= 0 selects 1/sqrt(dk).
  *   rows: flat row ids (b*H + h)*Lq + i, in non-decreasing (b, h) order, or
@@ -269,9 +290,9 @@ static int run_threads(void *(*fn)(void *), void *job, int nthreads)
  * Returns 0, or a negative error code.
  */
 int oracle_attention(int elem_is_bf16, const void *Q, const void *K, const void *V, int B, int H,
-                     int Lq, int Lk, int dk, int dv, int mask_kind, const int32_t *kv_lens,
-                     double scale, const int64_t *rows, int64_t nrows, double *O, double *LSE,
-                     double *A, int nthreads)
+                     int Hkv, int Lq, int Lk, int dk, int dv, int mask_kind,
+                     const int32_t *kv_lens, double scale, const int64_t *rows, int64_t nrows,
+                     double *O, double *LSE, double *A, int nthreads)
 {
     attn_job J;
     int64_t r, n_units = 0;
@@ -279,7 +300,11 @@ int oracle_attention(int elem_is_bf16, const void *Q, const void *K, const void 
     int rc;
     if (!Q || !K || !V || !O || !LSE || B < 0 || H < 0 || Lq < 0 || Lk < 0 || dk < 1 || dv < 1)
         return OR_ERR_ARG;
-    if ((mask_kind & ~(OR_MASK_CAUSAL | OR_MASK_PADDING)) != 0)
+    if (Hkv < 1 || (H > 0 && H % Hkv != 0))
+        return OR_ERR_ARG;
+    if ((mask_kind & ~(OR_MASK_CAUSAL | OR_MASK_PADDING | OR_MASK_CAUSAL_BR)) != 0)
+        return OR_ERR_ARG;
+    if ((mask_kind & OR_MASK_CAUSAL) && (mask_kind & OR_MASK_CAUSAL_BR))
         return OR_ERR_ARG;
     if (mask_kind & OR_MASK_PADDING) {
         int b;
@@ -305,6 +330,7 @@ int oracle_attention(int elem_is_bf16, const void *Q, const void *K, const void 
     J.V = V;
     J.B = B;
     J.H = H;
+    J.Hkv = Hkv;
     J.Lq = Lq;
     J.Lk = Lk;
     J.dk = dk;
@@ -420,7 +446,7 @@ static void *layer_worker(void *arg)
             l = (int)(id % J->L);
             slot = J->batch_slot[b];
             kv_len = (J->mask_kind & OR_MASK_PADDING) ? J->kv_lens[b] : J->L;
-            n_keys = valid_keys(l, J->L, J->mask_kind, kv_len);
+            n_keys = valid_keys(l, J->L, J->L, J->mask_kind, kv_len);
             /* step 1 for the query: q = x W_Q */
             for (c = 0; c < dm; ++c)
                 x[c] = widen_bf16(J->X[((size_t)b * J->L + l) * dm + c]);
@@ -533,7 +559,7 @@ int oracle_mha_layer(const uint16_t *X, const uint16_t *Wqkv, const uint16_t *Wo
         int64_t id = rows ? rows[r] : r;
         int bb = (int)(id / L), l = (int)(id % L);
         int kv_len = (mask_kind & OR_MASK_PADDING) ? kv_lens[bb] : L;
-        int nk = valid_keys(l, L, mask_kind, kv_len);
+        int nk = valid_keys(l, L, L, mask_kind, kv_len);
         if (J.batch_slot[bb] < 0) {
             J.batch_slot[bb] = J.n_slots;
             J.slot_batch[J.n_slots] = bb;

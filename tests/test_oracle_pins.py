@@ -370,6 +370,65 @@ def selected_rows_match_full_run(orc):
 
 
 # ---------------------------------------------------------------------------
+# grouped-query attention and the bottom-right causal mask
+# ---------------------------------------------------------------------------
+@pin
+def grouped_query_attention_is_shared_kv_heads(orc):
+    """P-e "MHA -> MQA -> GQA -> MLA": each run of h/g query heads shares one
+    K/V head (g = h is MHA, g = 1 is MQA).  Replicating each K/V head over its
+    query heads and running plain MHA must give the same bits; PyTorch's own
+    SDPA with enable_gqa agrees in float64."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    B, H, L, dk = 2, 6, 33, 16
+    q = _rand((B, H, L, dk), 171)
+    for Hkv in (6, 3, 2, 1):
+        k = _rand((B, Hkv, L, dk), 172 + Hkv)
+        v = _rand((B, Hkv, L, 8), 173 + Hkv)
+        rep_k = np.repeat(k, H // Hkv, axis=1)
+        rep_v = np.repeat(v, H // Hkv, axis=1)
+        for mk in (MASK_NONE, MASK_CAUSAL):
+            O, Lse = orc.attention(q, k, v, mask_kind=mk)
+            Or, Lr = orc.attention(q, rep_k, rep_v, mask_kind=mk)
+            assert np.array_equal(O, Or) and np.array_equal(Lse, Lr)
+            try:
+                tO = F.scaled_dot_product_attention(
+                    torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v),
+                    is_causal=bool(mk & MASK_CAUSAL), enable_gqa=True).numpy()
+            except TypeError:  # torch without enable_gqa
+                continue
+            np.testing.assert_allclose(O, tO, atol=1e-12)
+
+
+@pin
+def bottom_right_causal_mask(orc):
+    """Causal mask aligned to the last key (query i at key position
+    i + Lk - Lq): equal to the ordinary causal mask when Lq = Lk, to no mask for
+    a single query, and to PyTorch SDPA with the explicit lower-right mask."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    BR = 4
+    q, k, v = _case(181, Lq=29, Lk=29)
+    a = orc.attention(q, k, v, mask_kind=BR)
+    b = orc.attention(q, k, v, mask_kind=MASK_CAUSAL)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    q1, k1, v1 = _case(182, Lq=1, Lk=40)
+    a = orc.attention(q1, k1, v1, mask_kind=BR)
+    b = orc.attention(q1, k1, v1)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    for Lq, Lk in ((7, 30), (30, 7)):
+        q2, k2, v2 = _case(183 + Lq, Lq=Lq, Lk=Lk)
+        O, Lse = orc.attention(q2, k2, v2, mask_kind=BR)
+        keep = np.tril(np.ones((Lq, Lk), dtype=bool), Lk - Lq)
+        live = keep.any(axis=1)
+        tO = F.scaled_dot_product_attention(torch.from_numpy(q2), torch.from_numpy(k2),
+                                            torch.from_numpy(v2),
+                                            attn_mask=torch.from_numpy(keep)).numpy()
+        np.testing.assert_allclose(O[:, :, live], tO[:, :, live], atol=1e-12)
+        assert np.all(O[:, :, ~live] == 0.0) and np.all(np.isneginf(Lse[:, :, ~live]))
+
+
+# ---------------------------------------------------------------------------
 # the five-step layer
 # ---------------------------------------------------------------------------
 def _layer_case(seed, B=2, L=19, dm=24, H=3):
@@ -514,6 +573,10 @@ MUTANTS = [
     ("layer_heads_share_keys",
      "const double *Kh = J->Kp + (size_t)slot * J->L * dm + (size_t)head * dk;",
      "const double *Kh = J->Kp + (size_t)slot * J->L * dm;"),
+    ("gqa_heads_not_grouped", "kvbh = (int64_t)b * J->Hkv + (int)(bh % J->H) / (J->H / J->Hkv);",
+     "kvbh = (int64_t)b * J->Hkv + (int)(bh % J->H) % J->Hkv;"),
+    ("causal_br_offset_sign", "long long lim = (long long)i + 1 + (long long)Lk - (long long)Lq;",
+     "long long lim = (long long)i + 1 + (long long)Lq - (long long)Lk;"),
     ("layer_wo_transposed", "J.Wo_d[(size_t)c * dm + n] = widen_bf16(Wo[(size_t)c * dm + n]);",
      "J.Wo_d[(size_t)n * dm + c] = widen_bf16(Wo[(size_t)c * dm + n]);"),
 ]
