@@ -52,8 +52,23 @@ typedef enum {
                                 mha_layer_fwd_noalloc                       */
 } attn_status_t;
 
-/* mask_kind bit flags; ATTN_MASK_CAUSAL | ATTN_MASK_PADDING applies both */
-enum { ATTN_MASK_NONE = 0, ATTN_MASK_CAUSAL = 1, ATTN_MASK_PADDING = 2 };
+/*
+ * mask_kind bit flags.  PADDING combines with either causal flag; the two
+ * causal flags are exclusive.
+ *   ATTN_MASK_CAUSAL: key j is hidden from query i when j > i (the look-ahead
+ *     mask, aligned to the first key).
+ *   ATTN_MASK_CAUSAL_BOTTOM_RIGHT: key j is hidden from query i when
+ *     j > i + (Lk - Lq): the same mask aligned to the last key, for Lq queries
+ *     that continue a sequence of Lk keys which includes them (e.g. decoding
+ *     against a KV cache).  Equal to ATTN_MASK_CAUSAL when Lq == Lk; a query
+ *     with no visible key (Lq > Lk) gets O = 0, LSE = -inf.
+ */
+enum {
+  ATTN_MASK_NONE = 0,
+  ATTN_MASK_CAUSAL = 1,
+  ATTN_MASK_PADDING = 2,
+  ATTN_MASK_CAUSAL_BOTTOM_RIGHT = 4
+};
 
 /*
  * attn_fwd -- multi-head attention forward over [B, h, L, d] heads.
@@ -65,8 +80,7 @@ enum { ATTN_MASK_NONE = 0, ATTN_MASK_CAUSAL = 1, ATTN_MASK_PADDING = 2 };
  *   kv_lens int32 [B] device array, required iff mask_kind has the PADDING
  *     bit: sequence b's valid length.  Keys j >= kv_lens[b] are masked; query
  *     rows i >= kv_lens[b] are padding and get O = 0, LSE = -inf.
- *   mask_kind: ATTN_MASK_* flags.  CAUSAL hides key j from query i when j > i
- *     (top-left aligned when Lq != Lk).
+ *   mask_kind: ATTN_MASK_* flags (see above).
  *   scale: multiplier of Q K^T; scale <= 0 selects 1 / sqrt(d_k).
  *   A row with no visible key (kv_lens[b] == 0, or Lk == 0) gets O = 0 and
  *   LSE = -inf.  The attention matrix itself is never formed or returned.
@@ -80,6 +94,40 @@ enum { ATTN_MASK_NONE = 0, ATTN_MASK_CAUSAL = 1, ATTN_MASK_PADDING = 2 };
 attn_status_t attn_fwd(const void* Q, const void* K, const void* V, int B, int h, int Lq, int Lk,
                        int d_k, int d_v, int mask_kind, const int32_t* kv_lens, float scale,
                        void* O, float* LSE, void* stream);
+
+/*
+ * attn_fwd_gqa -- attn_fwd with grouped-query attention ("Self-Attention 机制",
+ * section "MHA -> MQA -> GQA -> MLA"): h query heads share h_kv key/value
+ * heads, each run of h/h_kv consecutive query heads reading one K/V head
+ * (query head i reads K/V head i / (h/h_kv)).  h_kv == h is attn_fwd (multi-
+ * head), h_kv == 1 is multi-query attention.
+ *
+ *   Q bf16 [B, h, Lq, d_k]; K bf16 [B, h_kv, Lk, d_k]; V bf16 [B, h_kv, Lk, d_v];
+ *   O, LSE, kv_lens, mask_kind, scale, alignment and errors as for attn_fwd;
+ *   h must be a multiple of h_kv (else ATTN_ERR_INVALID_ARG).
+ */
+attn_status_t attn_fwd_gqa(const void* Q, const void* K, const void* V, int B, int h, int h_kv,
+                           int Lq, int Lk, int d_k, int d_v, int mask_kind,
+                           const int32_t* kv_lens, float scale, void* O, float* LSE,
+                           void* stream);
+
+/*
+ * attn_weights -- the attention matrix A for inspection of small problems.
+ * The pages' reference snippets return A = softmax(Q K^T / sqrt(d_k) + M) next
+ * to the output ("attention-mechanism" page, section "最小实现";
+ * "多模态大模型学习笔记（十四）", section 2.3); attn_fwd never forms it.  This
+ * call rebuilds it from the LSE that attn_fwd / attn_fwd_gqa returned for the
+ * same Q, K, mask and scale: A_ij = exp(scale * q_i . k_j - LSE_i) for a
+ * visible key j and 0 for a masked one (rows with LSE = -inf are all 0).
+ *
+ *   Q bf16 [B, h, Lq, d_k]; K bf16 [B, h_kv, Lk, d_k]; LSE float [B, h, Lq];
+ *   A float [B, h, Lq, Lk] (written).  mask_kind, kv_lens, scale as for
+ *   attn_fwd.  d_k <= 256.  It is a plain CUDA-core kernel (one thread per
+ *   entry, no tensor cores), meant for shapes small enough to inspect.
+ */
+attn_status_t attn_weights(const void* Q, const void* K, const float* LSE, int B, int h,
+                           int h_kv, int Lq, int Lk, int d_k, int mask_kind,
+                           const int32_t* kv_lens, float scale, float* A, void* stream);
 
 /*
  * mha_layer_workspace_bytes -- device workspace mha_layer_fwd needs for this

@@ -141,22 +141,24 @@ def attn_flops(B, H, Lq, Lk, d, mask_kind, kv_lens=None) -> float:
 # generators
 # ---------------------------------------------------------------------------
 def make_attention_inputs(B, H, Lq, Lk, d_k, d_v, seed, kv_len_range=None,
-                          boost_frac=0.0, boost=1.0, kv_lens=None):
+                          boost_frac=0.0, boost=1.0, kv_lens=None, H_kv=None):
     """Draw Q, K, V ~ N(0,1) (float32), optionally scale a random subset of key
-    rows per head by ``boost``, then round to bfloat16.
+    rows per head by ``boost``, then round to bfloat16.  ``H_kv`` (default H)
+    is the number of K/V heads (grouped-query attention).
 
     Draw order: Q, K, V, then the boosted key rows (per (b, h) in order), then
     the per-sequence valid lengths.  Returns a dict of uint16 bit arrays and
     ``kv_lens`` (int32 [B] or None).
     """
     rng = np.random.default_rng(seed)
+    Hk = H if H_kv is None else H_kv
     q = rng.standard_normal((B, H, Lq, d_k), dtype=np.float32)
-    k = rng.standard_normal((B, H, Lk, d_k), dtype=np.float32)
-    v = rng.standard_normal((B, H, Lk, d_v), dtype=np.float32)
+    k = rng.standard_normal((B, Hk, Lk, d_k), dtype=np.float32)
+    v = rng.standard_normal((B, Hk, Lk, d_v), dtype=np.float32)
     if boost_frac > 0.0:
         nb = int(round(boost_frac * Lk))
         for b in range(B):
-            for h in range(H):
+            for h in range(Hk):
                 rows = rng.choice(Lk, nb, replace=False)
                 k[b, h, rows, :] *= np.float32(boost)
     if kv_lens is None and kv_len_range is not None:

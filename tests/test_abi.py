@@ -35,7 +35,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ["attn_fwd", "mha_layer_fwd", "mha_layer_workspace_bytes", "attn_check_device_status",
+    for n in ["attn_fwd", "attn_fwd_gqa", "mha_layer_fwd", "mha_layer_workspace_bytes", "attn_check_device_status",
               "attn_status_string", "attn_gemm_bf16", "attn_set_wait_limit_ns",
               "attn_debug_skip_kv_load"]:
         assert n in names, n
@@ -69,7 +69,8 @@ def test_host_validation_before_any_cuda_call(cdll):
     INVALID, UNSUPPORTED, MISALIGNED = 1, 2, 3
     # negative sizes, unknown mask bits, NaN scale
     assert f(p, p, p, -1, 1, 8, 8, 64, 64, 0, None, 0.0, p, None, None) == INVALID
-    assert f(p, p, p, 1, 1, 8, 8, 64, 64, 4, None, 0.0, p, None, None) == INVALID
+    assert f(p, p, p, 1, 1, 8, 8, 64, 64, 8, None, 0.0, p, None, None) == INVALID
+    assert f(p, p, p, 1, 1, 8, 8, 64, 64, 5, None, 0.0, p, None, None) == INVALID  # both causal
     assert f(p, p, p, 1, 1, 8, 8, 64, 64, 0, None, float("nan"), p, None, None) == INVALID
     # head dims this build does not implement
     assert f(p, p, p, 1, 1, 8, 8, 96, 96, 0, None, 0.0, p, None, None) == UNSUPPORTED
@@ -105,3 +106,14 @@ def test_layer_and_gemm_validation(cdll):
     g.argtypes = [vp, vp, vp, i, i, i, vp]
     assert g(p, p, p, 100, 256, 64, None) == 2
     assert g(p, p, p, -1, 256, 64, None) == 1
+
+
+def test_gqa_validation(cdll):
+    f = cdll.attn_fwd_gqa
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    f.restype = i
+    f.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp, ctypes.c_float, vp, vp, vp]
+    p = ctypes.c_void_p(0x1000)
+    assert f(p, p, p, 1, 8, 3, 8, 8, 64, 64, 0, None, 0.0, p, None, None) == 1  # 8 % 3
+    assert f(p, p, p, 1, 8, 0, 8, 8, 64, 64, 0, None, 0.0, p, None, None) == 1
+    assert f(None, None, None, 1, 8, 2, 0, 8, 64, 64, 0, None, 0.0, None, None, None) == 0

@@ -139,3 +139,68 @@ def test_large_workloads_sampled(cuda_lib, name, rows_per_head):
     compare_attention(O.reshape(-1, w.d_v)[flat], L.reshape(-1)[flat], Or, Lr, name)
     # causal row 0 of every head attends only to key 0: O_0 = V_0 exactly
     assert np.array_equal(O[:, :, 0, :], bf16_to_f32(inp["v"][:, :, 0, :]))
+
+
+MASK_BR = 4  # causal, aligned to the last key
+
+GQA = [(2, 8, 8, 300, 300, 128), (1, 8, 2, 257, 257, 64), (2, 6, 1, 200, 200, 128),
+       (1, 16, 4, 1000, 1000, 128), (1, 8, 4, 64, 900, 64)]
+
+
+@pytest.mark.parametrize("shape", GQA, ids=["x".join(map(str, s)) for s in GQA])
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_CAUSAL | MASK_PADDING, MASK_BR],
+                         ids=["none", "causal", "causal+pad", "causal_br"])
+def test_grouped_query_attention(cuda_lib, shape, mask):
+    """h query heads over h_kv K/V heads ("Self-Attention 机制", MHA -> MQA ->
+    GQA -> MLA): h_kv = h is MHA, h_kv = 1 is MQA."""
+    B, H, Hkv, Lq, Lk, d = shape
+    inp = make_attention_inputs(B, H, Lq, Lk, d, d, seed=7 * Lq + Hkv, H_kv=Hkv)
+    inp["kv_lens"] = _kv_lens(B, Lk, 5, [Lk - 3, Lk // 2])
+    O, L = _run(cuda_lib, inp, mask)
+    Or, Lr = oracle.attention(inp["q"], inp["k"], inp["v"], mask_kind=mask,
+                              kv_lens=inp["kv_lens"])
+    compare_attention(O, L, Or, Lr, "gqa %s mask=%d" % (shape, mask))
+
+
+BR = [(1, 2, 1, 700, 64), (2, 2, 64, 1000, 128), (1, 3, 300, 300, 128), (2, 2, 300, 100, 64),
+      (1, 1, 129, 513, 128), (1, 2, 255, 4096, 128)]
+
+
+@pytest.mark.parametrize("shape", BR, ids=["x".join(map(str, s)) for s in BR])
+@pytest.mark.parametrize("mask", [MASK_BR, MASK_BR | MASK_PADDING], ids=["br", "br+pad"])
+def test_bottom_right_causal(cuda_lib, shape, mask):
+    """Causal mask aligned to the last key: Lq queries continuing an Lk-key
+    sequence (query i sees keys j <= i + Lk - Lq); rows with no key are 0."""
+    B, H, Lq, Lk, d = shape
+    inp = make_attention_inputs(B, H, Lq, Lk, d, d, seed=13 * Lq + Lk)
+    inp["kv_lens"] = _kv_lens(B, Lk, 9, [Lk, max(Lk - 50, 1)])
+    O, L = _run(cuda_lib, inp, mask)
+    Or, Lr = oracle.attention(inp["q"], inp["k"], inp["v"], mask_kind=mask,
+                              kv_lens=inp["kv_lens"])
+    compare_attention(O, L, Or, Lr, "causal_br %s mask=%d" % (shape, mask))
+
+
+WEIGHTS = [(1, 2, 37, 37, 64, MASK_NONE), (2, 2, 130, 130, 128, MASK_CAUSAL),
+           (2, 1, 70, 90, 64, MASK_PADDING), (1, 2, 20, 50, 128, MASK_BR)]
+
+
+@pytest.mark.parametrize("shape", WEIGHTS, ids=["x".join(map(str, s)) for s in WEIGHTS])
+def test_attention_weights(cuda_lib, shape):
+    """A rebuilt from the forward LSE matches the oracle's A entry by entry
+    (|err| <= 1e-4: fp32 scores and LSE, entries in [0, 1]); rows sum to 1 and
+    masked entries are exactly 0."""
+    import torch
+    B, H, Lq, Lk, d, mask = shape
+    inp = make_attention_inputs(B, H, Lq, Lk, d, d, seed=Lq * 3 + Lk)
+    inp["kv_lens"] = _kv_lens(B, Lk, 2, [Lk - 5, Lk // 3])
+    kv = torch.from_numpy(inp["kv_lens"]).cuda() if mask & MASK_PADDING else None
+    q, k, v = up(inp["q"]), up(inp["k"]), up(inp["v"])
+    O, L = cuda_lib.attn_fwd(q, k, v, mask_kind=mask, kv_lens=kv)
+    A = cuda_lib.attn_weights(q, k, L, mask_kind=mask, kv_lens=kv).cpu().numpy()
+    cuda_lib.check_device_status()
+    _, Lr, Ar = oracle.attention(inp["q"], inp["k"], inp["v"], mask_kind=mask,
+                                 kv_lens=inp["kv_lens"], want_weights=True)
+    assert np.abs(A - Ar).max() <= 1e-4
+    assert np.all(A[Ar == 0.0] == 0.0)
+    live = np.isfinite(Lr)
+    np.testing.assert_allclose(A.sum(-1)[live], 1.0, atol=1e-3)

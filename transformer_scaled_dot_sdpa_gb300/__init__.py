@@ -18,7 +18,8 @@ import os
 import torch
 
 __all__ = [
-    "MASK_NONE", "MASK_CAUSAL", "MASK_PADDING", "AttnError", "attn_fwd", "mha_layer_fwd",
+    "MASK_NONE", "MASK_CAUSAL", "MASK_PADDING", "MASK_CAUSAL_BOTTOM_RIGHT", "AttnError", "attn_fwd",
+    "attn_weights", "mha_layer_fwd",
     "mha_layer_workspace_bytes", "mha_layer_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gemm_bf16",
     "check_device_status", "set_wait_limit_ns",
     "debug_skip_kv_load", "library_path", "lib",
@@ -27,6 +28,7 @@ __all__ = [
 MASK_NONE = 0
 MASK_CAUSAL = 1
 MASK_PADDING = 2
+MASK_CAUSAL_BOTTOM_RIGHT = 4
 
 ATTN_OK = 0
 STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
@@ -57,6 +59,11 @@ def _load():
                              ctypes.c_size_t)
     L.attn_fwd.restype = i32
     L.attn_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp, vp]
+    L.attn_fwd_gqa.restype = i32
+    L.attn_fwd_gqa.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp,
+                               vp, vp]
+    L.attn_weights.restype = i32
+    L.attn_weights.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp]
     L.mha_layer_workspace_bytes.restype = sz
     L.mha_layer_workspace_bytes.argtypes = [i32, i32, i32, i32]
     L.mha_layer_fwd.restype = i32
@@ -107,15 +114,16 @@ def attn_fwd(q, k, v, mask_kind=MASK_NONE, kv_lens=None, scale=None, out=None, l
              return_lse=True, stream=None):
     """Multi-head attention forward: softmax(Q K^T * scale + M) V.
 
-    q [B,h,Lq,d], k [B,h,Lk,d], v [B,h,Lk,d] bf16 CUDA tensors; ``kv_lens``
-    int32 [B] (padding mask); ``scale`` None -> 1/sqrt(d).  Returns
+    q [B,h,Lq,d], k [B,h_kv,Lk,d], v [B,h_kv,Lk,d] bf16 CUDA tensors (h_kv
+    divides h: grouped-query attention when h_kv < h); ``kv_lens`` int32 [B]
+    (padding mask); ``scale`` None -> 1/sqrt(d).  Returns
     (O bf16 [B,h,Lq,d], LSE fp32 [B,h,Lq] or None).
     """
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _dev_tensor(t, n, torch.bfloat16)
     B, h, Lq, dk = q.shape
-    Lk, dv = k.shape[2], v.shape[3]
-    if tuple(k.shape) != (B, h, Lk, dk) or tuple(v.shape) != (B, h, Lk, dv):
+    h_kv, Lk, dv = k.shape[1], k.shape[2], v.shape[3]
+    if tuple(k.shape) != (B, h_kv, Lk, dk) or tuple(v.shape) != (B, h_kv, Lk, dv):
         raise ValueError("q/k/v shapes do not match")
     if out is None:
         out = torch.empty((B, h, Lq, dv), dtype=torch.bfloat16, device=q.device)
@@ -128,11 +136,38 @@ def attn_fwd(q, k, v, mask_kind=MASK_NONE, kv_lens=None, scale=None, out=None, l
         _dev_tensor(lse, "lse", torch.float32)
     if kv_lens is not None:
         _dev_tensor(kv_lens, "kv_lens", torch.int32)
-    st = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, h, Lq, Lk, dk, dv, int(mask_kind),
-                      _ptr(kv_lens), float(scale) if scale else 0.0, _ptr(out), _ptr(lse),
-                      _stream_handle(stream))
-    _check(st, "attn_fwd")
+    if h_kv == h:
+        st = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, h, Lq, Lk, dk, dv, int(mask_kind),
+                          _ptr(kv_lens), float(scale) if scale else 0.0, _ptr(out), _ptr(lse),
+                          _stream_handle(stream))
+        _check(st, "attn_fwd")
+    else:
+        st = lib.attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), B, h, h_kv, Lq, Lk, dk, dv,
+                              int(mask_kind), _ptr(kv_lens), float(scale) if scale else 0.0,
+                              _ptr(out), _ptr(lse), _stream_handle(stream))
+        _check(st, "attn_fwd_gqa")
     return out, lse
+
+
+def attn_weights(q, k, lse, mask_kind=MASK_NONE, kv_lens=None, scale=None, out=None,
+                 stream=None):
+    """Attention matrix A [B,h,Lq,Lk] (fp32) rebuilt from attn_fwd's LSE, for
+    inspecting small problems: A_ij = exp(scale q_i.k_j - LSE_i), 0 if masked."""
+    _dev_tensor(q, "q", torch.bfloat16)
+    _dev_tensor(k, "k", torch.bfloat16)
+    _dev_tensor(lse, "lse", torch.float32)
+    B, h, Lq, dk = q.shape
+    h_kv, Lk = k.shape[1], k.shape[2]
+    if out is None:
+        out = torch.empty((B, h, Lq, Lk), dtype=torch.float32, device=q.device)
+    _dev_tensor(out, "out", torch.float32)
+    if kv_lens is not None:
+        _dev_tensor(kv_lens, "kv_lens", torch.int32)
+    st = lib.attn_weights(_ptr(q), _ptr(k), _ptr(lse), B, h, h_kv, Lq, Lk, dk, int(mask_kind),
+                          _ptr(kv_lens), float(scale) if scale else 0.0, _ptr(out),
+                          _stream_handle(stream))
+    _check(st, "attn_weights")
+    return out
 
 
 def mha_layer_workspace_bytes(B, L, d_model, h):

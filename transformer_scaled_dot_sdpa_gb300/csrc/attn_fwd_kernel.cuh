@@ -64,6 +64,8 @@ enum : int { ATTN_MASK_CAUSAL_BIT = 1, ATTN_MASK_PADDING_BIT = 2 };
 
 struct AttnParams {
   int B, H, Lq, Lk;
+  int kv_group;            // query heads per K/V head (grouped-query attention)
+  int causal_offset;       // causal: query i sees keys j <= i + causal_offset
   int mask_kind;           // bit 0 causal, bit 1 padding
   int packed;              // 0: Q/K/V maps over [B,H,L,d]; 1: over [B,L,3,H,d]
   const int32_t* kv_lens;  // [B] valid lengths (padding) or nullptr
@@ -105,6 +107,7 @@ struct AttnLayout {
 
 struct AttnItem {
   int b, h;
+  int kvh;                // K/V head read by query head h
   int row0[ATTN_QTILES];  // first query row of each Q tile
   int nkv[ATTN_QTILES];   // KV tiles each Q tile needs (0: nothing to compute)
   int nkv_max;
@@ -127,6 +130,7 @@ __device__ __forceinline__ bool attn_get_item(const AttnParams& p, int k, AttnIt
   const int qb = p.n_qblocks - 1 - rank;
   it.b = bh / p.H;
   it.h = bh - it.b * p.H;
+  it.kvh = it.h / p.kv_group;
   int kv_len = p.Lk;
   it.kv_len_raw = p.Lk;
   if (p.mask_kind & ATTN_MASK_PADDING_BIT) {
@@ -146,7 +150,7 @@ __device__ __forceinline__ bool attn_get_item(const AttnParams& p, int k, AttnIt
       int lim = kv_len;
       if (p.mask_kind & ATTN_MASK_CAUSAL_BIT) {
         const int last = min(r0 + ATTN_BLOCK_M - 1, p.Lq - 1);
-        lim = min(lim, last + 1);
+        lim = min(lim, max(last + 1 + p.causal_offset, 0));
       }
       n = (lim + ATTN_BLOCK_N - 1) / ATTN_BLOCK_N;
     }
@@ -204,12 +208,12 @@ __device__ __forceinline__ void attn_tma_role(const CUtensorMap* tmQ, const CUte
         mbar_arrive_expect_tx(&bars[L::B_K_FULL + s], L::TILE_BYTES);
         for (int c = 0; c < L::NCHUNK; ++c)
           attn_load_tile(tmK, smem + L::K_OFF + s * L::TILE_BYTES + c * L::CHUNK_BYTES,
-                         &bars[L::B_K_FULL + s], 64 * c, j * ATTN_BLOCK_N, it.h, it.b, p.packed);
+                         &bars[L::B_K_FULL + s], 64 * c, j * ATTN_BLOCK_N, it.kvh, it.b, p.packed);
       }
       mbar_arrive_expect_tx(&bars[L::B_V_FULL + s], L::TILE_BYTES);
       for (int c = 0; c < L::NCHUNK; ++c)
         attn_load_tile(tmV, smem + L::V_OFF + s * L::TILE_BYTES + c * L::CHUNK_BYTES,
-                       &bars[L::B_V_FULL + s], 64 * c, j * ATTN_BLOCK_N, it.h, it.b, p.packed);
+                       &bars[L::B_V_FULL + s], 64 * c, j * ATTN_BLOCK_N, it.kvh, it.b, p.packed);
     }
   }
   // Unwind: every load this thread issued must land before the CTA exits.
@@ -381,7 +385,7 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
     if (row0 >= p.Lq) continue;  // tile wholly past the end of the sequence
     const int r = row0 + rloc;
     int limit = it.kv_len;  // this row attends to keys [0, limit)
-    if (causal) limit = min(limit, r + 1);
+    if (causal) limit = min(limit, max(r + 1 + p.causal_offset, 0));
     const bool padded_row = padding && r >= it.kv_len;
     float m = -INFINITY, l = 0.f, lb = 0.f;
     for (int j = 0; j < nkv; ++j) {

@@ -11,6 +11,7 @@
 
 #include "../../include/gb300attn.h"
 #include "attn_fwd_kernel.cuh"
+#include "attn_weights_kernel.cuh"
 #include "gemm_kernel.cuh"
 
 namespace {
@@ -143,9 +144,9 @@ attn_status_t launch_attn(DeviceState* ds, int attr_idx, const CUtensorMap& mq,
 
 // Shared by attn_fwd and the layer: launch attention with prepared maps.
 attn_status_t run_attention(DeviceState* ds, const CUtensorMap& mq, const CUtensorMap& mk,
-                            const CUtensorMap& mv, int packed, int B, int H, int Lq, int Lk,
-                            int d, int mask_kind, const int32_t* kv_lens, float scale, void* O,
-                            long long osb, long long osh, long long osl, float* LSE,
+                            const CUtensorMap& mv, int packed, int B, int H, int H_kv, int Lq,
+                            int Lk, int d, int mask_kind, const int32_t* kv_lens, float scale,
+                            void* O, long long osb, long long osh, long long osl, float* LSE,
                             cudaStream_t stream) {
   gb300::AttnParams p;
   std::memset(&p, 0, sizeof p);
@@ -153,7 +154,11 @@ attn_status_t run_attention(DeviceState* ds, const CUtensorMap& mq, const CUtens
   p.H = H;
   p.Lq = Lq;
   p.Lk = Lk;
-  p.mask_kind = mask_kind;
+  p.kv_group = H / H_kv;
+  // both causal alignments are one bit in the kernel plus an offset
+  p.causal_offset = (mask_kind & ATTN_MASK_CAUSAL_BOTTOM_RIGHT) ? (Lk - Lq) : 0;
+  p.mask_kind = (mask_kind & ATTN_MASK_PADDING) |
+                ((mask_kind & (ATTN_MASK_CAUSAL | ATTN_MASK_CAUSAL_BOTTOM_RIGHT)) ? 1 : 0);
   p.packed = packed;
   p.kv_lens = kv_lens;
   const double sc = scale > 0.f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(d));
@@ -252,9 +257,21 @@ void attn_debug_skip_kv_load(long long index) {
 attn_status_t attn_fwd(const void* Q, const void* K, const void* V, int B, int h, int Lq, int Lk,
                        int d_k, int d_v, int mask_kind, const int32_t* kv_lens, float scale,
                        void* O, float* LSE, void* stream) {
+  return attn_fwd_gqa(Q, K, V, B, h, h, Lq, Lk, d_k, d_v, mask_kind, kv_lens, scale, O, LSE,
+                      stream);
+}
+
+attn_status_t attn_fwd_gqa(const void* Q, const void* K, const void* V, int B, int h, int h_kv,
+                           int Lq, int Lk, int d_k, int d_v, int mask_kind,
+                           const int32_t* kv_lens, float scale, void* O, float* LSE,
+                           void* stream) {
   // ---- host-side validation (no CUDA call before this point) ----
   if (B < 0 || h < 0 || Lq < 0 || Lk < 0) return ATTN_ERR_INVALID_ARG;
-  if ((mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_PADDING)) != 0) return ATTN_ERR_INVALID_ARG;
+  if (h_kv < 1 || (h > 0 && h % h_kv != 0)) return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_PADDING | ATTN_MASK_CAUSAL_BOTTOM_RIGHT)) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ATTN_MASK_CAUSAL) && (mask_kind & ATTN_MASK_CAUSAL_BOTTOM_RIGHT))
+    return ATTN_ERR_INVALID_ARG;
   if (!(scale == scale) || std::isinf(scale)) return ATTN_ERR_INVALID_ARG;
   if (d_k != d_v) return ATTN_ERR_UNSUPPORTED;
   if (d_k != 64 && d_k != 128) return ATTN_ERR_UNSUPPORTED;
@@ -282,10 +299,54 @@ attn_status_t attn_fwd(const void* Q, const void* K, const void* V, int B, int h
   }
   CUtensorMap mq, mk, mv;
   if ((st = map_bhld(&mq, Q, B, h, Lq, d_k)) != ATTN_OK) return st;
-  if ((st = map_bhld(&mk, K, B, h, Lk, d_k)) != ATTN_OK) return st;
-  if ((st = map_bhld(&mv, V, B, h, Lk, d_v)) != ATTN_OK) return st;
-  return run_attention(ds, mq, mk, mv, 0, B, h, Lq, Lk, d_k, mask_kind, kv_lens, scale, O, osb,
-                       osh, osl, LSE, s);
+  if ((st = map_bhld(&mk, K, B, h_kv, Lk, d_k)) != ATTN_OK) return st;
+  if ((st = map_bhld(&mv, V, B, h_kv, Lk, d_v)) != ATTN_OK) return st;
+  return run_attention(ds, mq, mk, mv, 0, B, h, h_kv, Lq, Lk, d_k, mask_kind, kv_lens, scale, O,
+                       osb, osh, osl, LSE, s);
+}
+
+attn_status_t attn_weights(const void* Q, const void* K, const float* LSE, int B, int h,
+                           int h_kv, int Lq, int Lk, int d_k, int mask_kind,
+                           const int32_t* kv_lens, float scale, float* A, void* stream) {
+  if (B < 0 || h < 0 || Lq < 0 || Lk < 0 || d_k < 1 || d_k > 256) return ATTN_ERR_INVALID_ARG;
+  if (h_kv < 1 || (h > 0 && h % h_kv != 0)) return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_PADDING | ATTN_MASK_CAUSAL_BOTTOM_RIGHT)) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ATTN_MASK_CAUSAL) && (mask_kind & ATTN_MASK_CAUSAL_BOTTOM_RIGHT))
+    return ATTN_ERR_INVALID_ARG;
+  if (!(scale == scale) || std::isinf(scale)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || h == 0 || Lq == 0 || Lk == 0) return ATTN_OK;
+  if (!Q || !K || !LSE || !A) return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ATTN_MASK_PADDING) && !kv_lens) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * h >= 65536 || static_cast<long long>(Lq) / 8 >= 65535)
+    return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(Q, 2) || !aligned(K, 2) || !aligned(LSE, 4) || !aligned(A, 4))
+    return ATTN_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  attn_status_t st = device_state(&ds, nullptr);
+  if (st != ATTN_OK) return st;
+  gb300::WeightsParams p;
+  p.Q = static_cast<const __nv_bfloat16*>(Q);
+  p.K = static_cast<const __nv_bfloat16*>(K);
+  p.LSE = LSE;
+  p.A = A;
+  p.B = B;
+  p.H = h;
+  p.Hkv = h_kv;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.d = d_k;
+  p.mask_kind = (mask_kind & ATTN_MASK_PADDING) |
+                ((mask_kind & (ATTN_MASK_CAUSAL | ATTN_MASK_CAUSAL_BOTTOM_RIGHT)) ? 1 : 0);
+  p.causal_offset = (mask_kind & ATTN_MASK_CAUSAL_BOTTOM_RIGHT) ? (Lk - Lq) : 0;
+  p.kv_lens = kv_lens;
+  p.scale = scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
+  const dim3 grid((Lk + gb300::WEIGHTS_TJ - 1) / gb300::WEIGHTS_TJ,
+                  (Lq + gb300::WEIGHTS_TI - 1) / gb300::WEIGHTS_TI, B * h);
+  const dim3 block(gb300::WEIGHTS_TJ, gb300::WEIGHTS_TI);
+  const size_t shm = static_cast<size_t>(gb300::WEIGHTS_TI + gb300::WEIGHTS_TJ) * d_k * sizeof(float);
+  gb300::attn_weights_kernel<<<grid, block, shm, static_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 size_t mha_layer_workspace_bytes(int B, int L, int d_model, int h) {
@@ -317,7 +378,10 @@ attn_status_t mha_layer_fwd(const void* X, const void* W_QKV, const void* W_O, i
                             float scale, void* Y, void* workspace, size_t workspace_bytes,
                             void* stream) {
   if (B < 0 || L < 0 || d_model <= 0 || h <= 0) return ATTN_ERR_INVALID_ARG;
-  if ((mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_PADDING)) != 0) return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_PADDING | ATTN_MASK_CAUSAL_BOTTOM_RIGHT)) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ATTN_MASK_CAUSAL) && (mask_kind & ATTN_MASK_CAUSAL_BOTTOM_RIGHT))
+    return ATTN_ERR_INVALID_ARG;
   if (!(scale == scale) || std::isinf(scale)) return ATTN_ERR_INVALID_ARG;
   if (d_model % h != 0) return ATTN_ERR_INVALID_ARG;
   const int dk = d_model / h;
@@ -350,7 +414,7 @@ attn_status_t mha_layer_fwd(const void* X, const void* W_QKV, const void* W_O, i
   if ((st = map_packed(&mq, qkv, B, h, L, dk)) != ATTN_OK) return st;
   if ((st = map_packed(&mk, qkv + blk, B, h, L, dk)) != ATTN_OK) return st;
   if ((st = map_packed(&mv, qkv + 2 * blk, B, h, L, dk)) != ATTN_OK) return st;
-  if ((st = run_attention(ds, mq, mk, mv, 1, B, h, L, L, dk, mask_kind, kv_lens, scale, cat,
+  if ((st = run_attention(ds, mq, mk, mv, 1, B, h, h, L, L, dk, mask_kind, kv_lens, scale, cat,
                           static_cast<long long>(L) * d_model, dk, d_model, nullptr, s)) !=
       ATTN_OK)
     return st;
