@@ -373,14 +373,155 @@ def ours_arm(args, w):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# the five-step layer workload
+# ---------------------------------------------------------------------------
+def layer_flops(w):
+    """8 N d^2 (QKV and W_O projections) + 4 N^2 d attention, causal-halved per
+    head ("Self-Attention 机制", section 瓶颈: the six matrix products)."""
+    N, dm = w.B * w.L, w.d_model
+    proj = 2.0 * N * dm * 3 * dm + 2.0 * N * dm * dm
+    attn = attn_flops(w.B, w.H, w.L, w.L, w.d_k, w.mask_kind)
+    return proj, attn
+
+
+def layer_arm(args, w):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import transformer_scaled_dot_sdpa_gb300 as g
+    inp = make_workload_inputs(replica_workload(w, rank))
+
+    def dev_bf16(bits, pin=False):
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory() if pin else t.to(dev)
+
+    hx = dev_bf16(inp["x"], pin=True)
+    x = hx.to(dev)
+    wqkv, wo = dev_bf16(inp["w_qkv"]), dev_bf16(inp["w_o"])
+    y = torch.empty_like(x)
+    ws = torch.empty(g.mha_layer_workspace_bytes(w.B, w.L, w.d_model, w.H), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        g.mha_layer_fwd(x, wqkv, wo, w.H, mask_kind=w.mask_kind, scale=w.scale, out=y,
+                        workspace=ws, stream=stream)
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / n
+
+    for _ in range(args.warmup):
+        step()
+    g.check_device_status(stream)
+    clocks = ClockSampler(dev.index if world == 1 else local)
+    clocks.start()
+    barrier(world)
+    ms = timed(step, args.steps)
+    barrier(world)
+    clk = clocks.stop()
+    g.check_device_status(stream)
+    ms_max = max_over_ranks(ms, world)
+
+    # each stage's kernel timed alone on the same shapes (for the roofline)
+    N, dm, dk = w.B * w.L, w.d_model, w.d_k
+    qkv = torch.empty((N, 3 * dm), dtype=torch.bfloat16, device=dev)
+    cat = torch.empty((N, dm), dtype=torch.bfloat16, device=dev)
+    x2 = x.view(N, dm)
+    ms_qkv = timed(lambda: g.gemm_bf16(x2, wqkv, out=qkv, stream=stream), args.steps)
+    ms_wo = timed(lambda: g.gemm_bf16(cat, wo, out=y.view(N, dm), stream=stream), args.steps)
+    qh = torch.empty((w.B, w.H, w.L, dk), dtype=torch.bfloat16, device=dev).normal_()
+    kh, vh = torch.empty_like(qh).normal_(), torch.empty_like(qh).normal_()
+    oh = torch.empty_like(qh)
+    ms_att = timed(lambda: g.attn_fwd(qh, kh, vh, mask_kind=w.mask_kind, scale=w.scale, out=oh,
+                                      return_lse=False, stream=stream), args.steps)
+    g.check_device_status(stream)
+
+    # end to end: X in from pinned host memory, Y back, every step
+    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        x.copy_(hx, non_blocking=True)
+        step()
+        hy.copy_(y, non_blocking=True)
+
+    e2e_step()
+    e2e_ms = max_over_ranks(timed(e2e_step, e2e_steps), world)
+
+    proj, attn = layer_flops(w)
+    flops = proj + attn
+    peaks, peak_src = load_peaks()
+    stages = {"qkv_gemm": (2.0 * N * dm * 3 * dm, ms_qkv), "attention": (attn, ms_att),
+              "wo_gemm": (2.0 * N * dm * dm, ms_wo)}
+    dom = max(stages, key=lambda k: stages[k][1])
+    achieved = stages[dom][0] / (stages[dom][1] * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "peak_source": "%s (bf16 dense burst)" % peak_src,
+                "kernel": {"qkv_gemm": "gemm_bf16_kernel", "wo_gemm": "gemm_bf16_kernel",
+                           "attention": "attn_fwd_kernel<%d>" % dk}[dom],
+                "stages_ms": {k: v[1] for k, v in stages.items()},
+                "stages_tflops": {k: v[0] / (v[1] * 1e-3) / 1e12 for k, v in stages.items()}}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        rows = np.arange(0, w.L, max(1, w.L // 64), dtype=np.int64)  # one sequence, 64 rows
+        t0 = time.perf_counter()
+        oracle.mha_layer(inp["x"], inp["w_qkv"], inp["w_o"], w.H, mask_kind=w.mask_kind,
+                         scale=w.scale, rows=rows)
+        dt = time.perf_counter() - t0
+        kv_proj = 2.0 * w.L * dm * 2 * dm          # K, V projections of the sequence
+        per_row = 2.0 * dm * dm * 2                 # Q and output projections
+        att = sum(4.0 * (int(r) + 1) * dk * w.H for r in rows)
+        fl = kv_proj + per_row * len(rows) + att
+        cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": oracle.default_threads(),
+               "kind": "oracle", "sample": "%d output rows of one sequence (K/V projections of "
+               "the whole sequence), %.3g FLOP in %.1f s" % (len(rows), fl, dt)}
+    line = {
+        "metric": METRIC, "value": world * flops / (ms_max * 1e-3) / 1e12, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "d_model": dm, "H": w.H,
+                   "mask": "causal" if w.mask_kind & MASK_CAUSAL else "none",
+                   "parallelism": "replicas x%d" % world,
+                   "l2": "no flush; X 34 MB, QKV workspace 101 MB, weights 8 MB"},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": int(hx.numel() * 2), "d2h_bytes_per_step": int(hy.numel() * 2),
+                "steps": e2e_steps, "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * args.steps,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=sorted(
-        n for n, w in WORKLOADS.items() if w.kind == "attn"))
+    ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-rows", type=int, default=65536,
                     help="query rows the CPU oracle baseline computes")
     ap.add_argument("--ref-rows", type=int, default=512,
@@ -390,6 +531,12 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
+    if w.kind == "layer":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the "
+                              "oracle on the attention workloads only"}))
+            return 0
+        return layer_arm(args, w)
     if args.impl == "reference":
         return reference_arm(args, w)
     return ours_arm(args, w)
