@@ -224,6 +224,37 @@ const char* attn_status_string(attn_status_t status);
 void attn_set_wait_limit_ns(uint64_t ns);
 
 /*
+ * Work schedules of the attention kernel.  Both compute the same function
+ * (online softmax over 128-key tiles, fp32 accumulation, bf16 P); they differ
+ * in how a CTA's work is laid out on the SM:
+ *   ATTN_SCHEDULE_TWO_QTILES  256 query rows per work item, Q in shared
+ *                             memory, one MMA issuer per 128-row tile
+ *   ATTN_SCHEDULE_ONE_QTILE   128 query rows per work item, Q and P in tensor
+ *                             memory, a double-buffered S, one issuer for
+ *                             Q K^T and another for P V, two softmax threads
+ *                             per query row
+ *   ATTN_SCHEDULE_SPLIT_KEYS  128 query rows per work item, its key tiles
+ *                             dealt alternately to two softmax warpgroups
+ *                             with separate accumulators, merged at the end
+ *                             of the item; issuers as in ONE_QTILE
+ *   ATTN_SCHEDULE_AUTO        the library picks one from the shape
+ */
+typedef enum {
+  ATTN_SCHEDULE_AUTO = 0,
+  ATTN_SCHEDULE_TWO_QTILES = 1,
+  ATTN_SCHEDULE_ONE_QTILE = 2,
+  ATTN_SCHEDULE_SPLIT_KEYS = 3
+} attn_schedule_t;
+
+/*
+ * attn_set_schedule -- schedule of later attention launches (attn_fwd,
+ * attn_fwd_gqa and the attention step of mha_layer_fwd / _noalloc); process-
+ * wide, like attn_set_wait_limit_ns.  Returns ATTN_ERR_INVALID_ARG (and keeps
+ * the current setting) for a value outside attn_schedule_t.
+ */
+attn_status_t attn_set_schedule(int schedule);
+
+/*
  * attn_debug_skip_kv_load -- testing hook: the next attn_fwd launches skip
  * the K-tile load with this running index in every CTA, so that a pipeline
  * wait runs out and the timeout path is exercised (-1 disables; the default).

@@ -29,3 +29,15 @@ def cuda_lib():
         pytest.fail("GPU test collected on a machine without a CUDA device")
     import transformer_scaled_dot_sdpa_gb300 as g
     return g
+
+
+# attention kernel schedules (attn_schedule_t): every parity test that uses
+# this fixture runs once per schedule
+SCHEDULES = {"two_qtiles": 1, "one_qtile": 2, "split_keys": 3}
+
+
+@pytest.fixture(params=list(SCHEDULES.values()), ids=list(SCHEDULES))
+def schedule(request, cuda_lib):
+    cuda_lib.set_schedule(request.param)
+    yield request.param
+    cuda_lib.set_schedule(cuda_lib.SCHEDULE_AUTO)

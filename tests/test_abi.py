@@ -117,3 +117,12 @@ def test_gqa_validation(cdll):
     assert f(p, p, p, 1, 8, 3, 8, 8, 64, 64, 0, None, 0.0, p, None, None) == 1  # 8 % 3
     assert f(p, p, p, 1, 8, 0, 8, 8, 64, 64, 0, None, 0.0, p, None, None) == 1
     assert f(None, None, None, 1, 8, 2, 0, 8, 64, 64, 0, None, 0.0, None, None, None) == 0
+
+
+def test_schedule_selection(cdll):
+    f = cdll.attn_set_schedule
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int]
+    for s in (1, 2, 3, 0):     # two Q tiles, one Q tile, split keys, automatic
+        assert f(s) == 0
+    assert f(4) == 1 and f(-1) == 1

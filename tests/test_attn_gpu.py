@@ -10,7 +10,7 @@ from sdpa_workloads import (MASK_CAUSAL, MASK_NONE, MASK_PADDING, WORKLOADS, bf1
                             make_attention_inputs, make_workload_inputs, sample_rows)
 from tests.parity_util import compare_attention, down, up
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("schedule")]
 
 ALL_MASKS = [MASK_NONE, MASK_CAUSAL, MASK_PADDING, MASK_CAUSAL | MASK_PADDING]
 

@@ -10,7 +10,7 @@ import oracle
 from sdpa_workloads import MASK_CAUSAL, make_attention_inputs
 from tests.parity_util import compare_attention, down, up
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("schedule")]
 
 ATTN_ERR_TIMEOUT = 5
 

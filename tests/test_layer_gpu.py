@@ -56,7 +56,7 @@ def _compare(Y, Yr, what):
                                       (2, 320, 768, 12)])
 @pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_PADDING,
                                   MASK_CAUSAL | MASK_PADDING])
-def test_layer_small(cuda_lib, B, L, dm, H, mask):
+def test_layer_small(cuda_lib, schedule, B, L, dm, H, mask):
     inp = make_layer_inputs(B, L, dm, seed=B * L + dm + mask, w_std=1.0 / np.sqrt(dm))
     kv = np.array([L, L // 3, 1, 0][:B], dtype=np.int32) if mask & MASK_PADDING else None
     Y = _layer_run(cuda_lib, inp, H, mask, kv)
@@ -67,7 +67,7 @@ def test_layer_small(cuda_lib, B, L, dm, H, mask):
             assert np.all(Y[b, kv[b]:] == 0.0)
 
 
-def test_layer_workload_sampled(cuda_lib):
+def test_layer_workload_sampled(cuda_lib, schedule):
     """The full layer workload (B=8, L=2048, d_model=1024, 16 heads, causal)
     in the benchmark's launch configuration; the oracle computes sampled rows
     of two sequences."""

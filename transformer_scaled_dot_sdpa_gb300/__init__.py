@@ -21,14 +21,20 @@ __all__ = [
     "MASK_NONE", "MASK_CAUSAL", "MASK_PADDING", "MASK_CAUSAL_BOTTOM_RIGHT", "AttnError", "attn_fwd",
     "attn_weights", "mha_layer_fwd",
     "mha_layer_workspace_bytes", "mha_layer_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gemm_bf16",
-    "check_device_status", "set_wait_limit_ns",
-    "debug_skip_kv_load", "library_path", "lib",
+    "check_device_status", "set_wait_limit_ns", "set_schedule", "SCHEDULE_AUTO",
+    "SCHEDULE_TWO_QTILES", "SCHEDULE_ONE_QTILE", "SCHEDULE_SPLIT_KEYS", "debug_skip_kv_load", "library_path", "lib",
 ]
 
 MASK_NONE = 0
 MASK_CAUSAL = 1
 MASK_PADDING = 2
 MASK_CAUSAL_BOTTOM_RIGHT = 4
+
+# attention work schedules (attn_schedule_t)
+SCHEDULE_AUTO = 0
+SCHEDULE_TWO_QTILES = 1
+SCHEDULE_ONE_QTILE = 2
+SCHEDULE_SPLIT_KEYS = 3
 
 ATTN_OK = 0
 STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
@@ -78,6 +84,8 @@ def _load():
     L.attn_status_string.argtypes = [i32]
     L.attn_set_wait_limit_ns.restype = None
     L.attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    L.attn_set_schedule.restype = i32
+    L.attn_set_schedule.argtypes = [i32]
     L.attn_debug_skip_kv_load.restype = None
     L.attn_debug_skip_kv_load.argtypes = [i64]
     return L
@@ -245,6 +253,11 @@ def check_device_status(stream=None):
 
 def set_wait_limit_ns(ns):
     lib.attn_set_wait_limit_ns(int(ns))
+
+
+def set_schedule(schedule):
+    """Select the attention kernel schedule of later launches (process-wide)."""
+    _check(lib.attn_set_schedule(int(schedule)), "attn_set_schedule")
 
 
 def debug_skip_kv_load(index):

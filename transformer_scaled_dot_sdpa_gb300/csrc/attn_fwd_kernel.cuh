@@ -272,91 +272,106 @@ template <int D>
 __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, uint8_t* smem,
                                               uint64_t* bars, uint32_t tmem, const WaitCtl& ctl,
                                               volatile int* tile0_started) {
+  // Run by a whole warp: every lane waits and computes the operands, one
+  // elected lane issues.  Operands computed by all lanes stay warp-uniform,
+  // which keeps the issue of each tcgen05.mma short.
   using L = AttnLayout<D>;
   constexpr uint32_t IDESC_S = idesc_bf16_f32(ATTN_BLOCK_M, ATTN_BLOCK_N, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(ATTN_BLOCK_M, D, true);
-  const uint32_t qa = smem_u32(smem + L::Q_OFF) + t * L::TILE_BYTES;
-  const uint32_t k_base = smem_u32(smem + L::K_OFF);
-  const uint32_t v_base = smem_u32(smem + L::V_OFF);
+  const uint64_t q_desc = smem_desc_sw128(smem_u32(smem + L::Q_OFF) + t * L::TILE_BYTES, 16, 1024);
+  const uint64_t k_desc = smem_desc_sw128(smem_u32(smem + L::K_OFF), 16, 1024);
+  const uint64_t v_desc = smem_desc_sw128(smem_u32(smem + L::V_OFF), L::CHUNK_BYTES, 1024);
   const uint32_t s_tmem = tmem + static_cast<uint32_t>(t * ATTN_BLOCK_N);
   const uint32_t p_tmem = s_tmem + 64u;  // P in the high half of the S columns
   const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(t * 128);
+  constexpr unsigned FULL = 0xffffffffu;
   uint32_t q_uses = 0, p_cnt = 0;
   uint32_t kv_it = 0;  // running KV tile index (stage = kv_it % STAGES)
   bool ok = true;
   AttnItem it;
+  // S_t = Q_t K^T for the K tile in stage s
+  auto issue_s = [&](int s) {
+    const uint64_t kd = k_desc + static_cast<uint64_t>((s * L::TILE_BYTES) >> 4);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::CHUNK_BYTES + (kk & 3) * 32) >> 4);
+      mma_bf16_ss(s_tmem, q_desc + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
+    }
+  };
   for (int k = 0; ok && attn_get_item(p, k, it); ++k) {
-    if (t == 0 && it.kv_len_raw != it.kv_len) atomicOr(p.status, ATTN_STATUS_BAD_KVLEN);
+    if (t == 0 && it.kv_len_raw != it.kv_len && elect_one())
+      atomicOr(p.status, ATTN_STATUS_BAD_KVLEN);
     if (it.nkv_max == 0) continue;
     const int nkv = t ? it.nkv[1] : it.nkv[0];
     // The two Q tiles' chains (S -> softmax -> P.V) are independent; tile 1
     // starts half a chain late so that the two softmax groups alternate on
     // the SM instead of competing.
-    if (t == 1 && k == 0 && it.nkv[0] > 0 && nkv > 0) ok = attn_wait_flag(tile0_started, ctl);
+    if (t == 1 && k == 0 && it.nkv[0] > 0 && nkv > 0)
+      ok = __all_sync(FULL, attn_wait_flag(tile0_started, ctl));
     // S_t(0)
     if (ok) {
       const int s = static_cast<int>(kv_it % L::STAGES);
-      ok = mbar_wait(&bars[L::B_K_FULL + s], (kv_it / L::STAGES) & 1u, ctl);
+      ok = __all_sync(FULL, mbar_wait(&bars[L::B_K_FULL + s], (kv_it / L::STAGES) & 1u, ctl));
       if (ok && nkv > 0) {
-        ok = mbar_wait(&bars[L::B_Q_FULL + t], q_uses & 1u, ctl);
+        ok = __all_sync(FULL, mbar_wait(&bars[L::B_Q_FULL + t], q_uses & 1u, ctl));
         ++q_uses;
         if (ok) {
           tc_fence_after();
-          const uint32_t ka = k_base + s * L::TILE_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * L::CHUNK_BYTES + (kk & 3) * 32;
-            mma_bf16_ss(s_tmem, smem_desc_sw128(qa + off, 16, 1024),
-                        smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          if (elect_one()) {
+            issue_s(s);
+            mma_commit(&bars[L::B_S_FULL + t]);
+            if (nkv == 1) mma_commit(&bars[L::B_Q_EMPTY + t]);
           }
-          mma_commit(&bars[L::B_S_FULL + t]);
-          if (nkv == 1) mma_commit(&bars[L::B_Q_EMPTY + t]);
+          __syncwarp();
         }
       }
     }
     for (int j = 0; ok && j < it.nkv_max; ++j, ++kv_it) {
       const int s = static_cast<int>(kv_it % L::STAGES);
-      ok = mbar_wait(&bars[L::B_V_FULL + s], (kv_it / L::STAGES) & 1u, ctl);
+      ok = __all_sync(FULL, mbar_wait(&bars[L::B_V_FULL + s], (kv_it / L::STAGES) & 1u, ctl));
       if (!ok) break;
       if (j < nkv) {
         // O_t += P_t(j) V_j
-        ok = mbar_wait(&bars[L::B_P_FULL + t], p_cnt & 1u, ctl);
+        ok = __all_sync(FULL, mbar_wait(&bars[L::B_P_FULL + t], p_cnt & 1u, ctl));
         if (!ok) break;
         ++p_cnt;
         tc_fence_after();
-        const uint32_t va = v_base + s * L::TILE_BYTES;
+        const uint64_t vd = v_desc + static_cast<uint64_t>((s * L::TILE_BYTES) >> 4);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < ATTN_BLOCK_N / 16; ++kk)
-          mma_bf16_ts(o_tmem, p_tmem + kk * 8, smem_desc_sw128(va + kk * 2048, L::CHUNK_BYTES, 1024),
-                      IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
-        // K_j (read by S_t(j), issued earlier) and V_j are free once this
-        // P.V completes; O_t is final after the item's last P.V
-        mma_commit(&bars[L::B_KV_EMPTY + s]);
-        if (j == nkv - 1) mma_commit(&bars[L::B_O_DONE + t]);
+          for (int kk = 0; kk < ATTN_BLOCK_N / 16; ++kk)
+            mma_bf16_ts(o_tmem, p_tmem + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4),
+                        IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+          // K_j (read by S_t(j), issued earlier) and V_j are free once this
+          // P.V completes; O_t is final after the item's last P.V
+          mma_commit(&bars[L::B_KV_EMPTY + s]);
+          if (j == nkv - 1) mma_commit(&bars[L::B_O_DONE + t]);
+        }
+        __syncwarp();
       } else {
-        mbar_arrive(&bars[L::B_KV_EMPTY + s]);
+        if (elect_one()) mbar_arrive(&bars[L::B_KV_EMPTY + s]);
+        __syncwarp();
       }
       if (j + 1 < it.nkv_max) {
         const int s1 = static_cast<int>((kv_it + 1) % L::STAGES);
-        ok = mbar_wait(&bars[L::B_K_FULL + s1], ((kv_it + 1) / L::STAGES) & 1u, ctl);
+        ok = __all_sync(FULL,
+                        mbar_wait(&bars[L::B_K_FULL + s1], ((kv_it + 1) / L::STAGES) & 1u, ctl));
         if (!ok) break;
         if (j + 1 < nkv) {
           // S_t(j+1) = Q_t K_{j+1}^T
-          const uint32_t ka = k_base + s1 * L::TILE_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * L::CHUNK_BYTES + (kk & 3) * 32;
-            mma_bf16_ss(s_tmem, smem_desc_sw128(qa + off, 16, 1024),
-                        smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          if (elect_one()) {
+            issue_s(s1);
+            mma_commit(&bars[L::B_S_FULL + t]);
+            if (j + 2 == nkv) mma_commit(&bars[L::B_Q_EMPTY + t]);
           }
-          mma_commit(&bars[L::B_S_FULL + t]);
-          if (j + 2 == nkv) mma_commit(&bars[L::B_Q_EMPTY + t]);
+          __syncwarp();
         }
       }
     }
   }
-  // Unwind: all MMAs issued by this thread complete before TMEM is freed.
-  mma_commit(&bars[L::B_DRAIN + t]);
+  // Unwind: all MMAs issued by this warp complete before TMEM is freed.
+  if (elect_one()) mma_commit(&bars[L::B_DRAIN + t]);
+  __syncwarp();
   mbar_wait_drain(&bars[L::B_DRAIN + t], 0u, ctl.limit_ns);
 }
 
@@ -600,8 +615,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     if (warp == 9) {
       if (lane == 0) attn_tma_role<D>(&tmQ, &tmK, &tmV, p, smem, bars, ctl);
     } else if (warp == 8 || warp == 10) {
-      if (lane == 0) attn_mma_role<D>(warp == 8 ? 0 : 1, p, smem, bars, tmem, ctl, tile0_started);
-      __syncwarp();
+      attn_mma_role<D>(warp == 8 ? 0 : 1, p, smem, bars, tmem, ctl, tile0_started);
     }
   } else {
     reg_alloc<ATTN_REGS_SOFTMAX>();

@@ -11,6 +11,8 @@
 
 #include "../../include/gb300attn.h"
 #include "attn_fwd_kernel.cuh"
+#include "attn_fwd_t1_kernel.cuh"
+#include "attn_fwd_t2_kernel.cuh"
 #include "attn_weights_kernel.cuh"
 #include "gemm_kernel.cuh"
 
@@ -33,7 +35,7 @@ struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   unsigned int* status = nullptr;
-  bool attn_attr[2] = {false, false};
+  bool attn_attr[6] = {false, false, false, false, false, false};
   bool gemm_attr = false;
   void* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch
 };
@@ -42,6 +44,7 @@ std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 unsigned long long g_wait_limit_ns = kDefaultWaitLimitNs;
 long long g_debug_skip_kv_load = -1;
+int g_schedule = ATTN_SCHEDULE_AUTO;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -119,26 +122,33 @@ attn_status_t map_packed(CUtensorMap* m, const void* base, int B, int H, int L, 
   return make_map_4d(m, base, dims, str, box);
 }
 
-template <int D>
-attn_status_t launch_attn(DeviceState* ds, int attr_idx, const CUtensorMap& mq,
-                          const CUtensorMap& mk, const CUtensorMap& mv, const gb300::AttnParams& p,
+template <int D, int SCHEDULE>
+attn_status_t launch_attn(DeviceState* ds, const CUtensorMap& mq, const CUtensorMap& mk,
+                          const CUtensorMap& mv, const gb300::AttnParams& p,
                           cudaStream_t stream) {
-  using L = gb300::AttnLayout<D>;
+  const int attr_idx = (D == 64 ? 0 : 1) + 2 * (SCHEDULE - 1);
+  const int smem = SCHEDULE == ATTN_SCHEDULE_ONE_QTILE    ? gb300::T1Layout<D>::SMEM_BYTES
+                   : SCHEDULE == ATTN_SCHEDULE_SPLIT_KEYS ? gb300::T2Layout<D>::SMEM_BYTES
+                                                          : gb300::AttnLayout<D>::SMEM_BYTES;
+  void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, gb300::AttnParams) =
+      SCHEDULE == ATTN_SCHEDULE_ONE_QTILE    ? gb300::attn_fwd_t1_kernel<D>
+      : SCHEDULE == ATTN_SCHEDULE_SPLIT_KEYS ? gb300::attn_fwd_t2_kernel<D>
+                                             : gb300::attn_fwd_kernel<D>;
   if (!ds->attn_attr[attr_idx]) {
-    // The kernel hands registers between warpgroups (setmaxnreg); the split
+    // The kernels hand registers between warpgroups (setmaxnreg); the split
     // adds up to exactly ATTN_THREADS x ATTN_REGS_AT_LAUNCH, so a build with a
     // different launch register count could wait forever: refuse it.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, gb300::attn_fwd_kernel<D>) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return ATTN_ERR_CUDA;
     if (fa.numRegs != gb300::ATTN_REGS_AT_LAUNCH || fa.maxThreadsPerBlock < gb300::ATTN_THREADS)
       return ATTN_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(gb300::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
       return ATTN_ERR_CUDA;
     ds->attn_attr[attr_idx] = true;
   }
   const int grid = p.n_items < ds->num_sms ? p.n_items : ds->num_sms;
-  gb300::attn_fwd_kernel<D><<<grid, gb300::ATTN_THREADS, L::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  kernel<<<grid, gb300::ATTN_THREADS, smem, stream>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -168,16 +178,29 @@ attn_status_t run_attention(DeviceState* ds, const CUtensorMap& mq, const CUtens
   p.o_stride_h = osh;
   p.o_stride_l = osl;
   p.LSE = LSE;
-  p.n_qblocks = (Lq + gb300::ATTN_ROWS_PER_ITEM - 1) / gb300::ATTN_ROWS_PER_ITEM;
-  p.n_items = static_cast<int>(static_cast<long long>(B) * H * p.n_qblocks);
   p.status = ds->status;
+  int schedule;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     p.wait_limit_ns = g_wait_limit_ns;
     p.debug_skip_kv_load = g_debug_skip_kv_load;
+    schedule = g_schedule;
   }
-  if (d == 64) return launch_attn<64>(ds, 0, mq, mk, mv, p, stream);
-  return launch_attn<128>(ds, 1, mq, mk, mv, p, stream);
+  if (schedule == ATTN_SCHEDULE_AUTO) schedule = ATTN_SCHEDULE_TWO_QTILES;
+  const int rows = schedule == ATTN_SCHEDULE_TWO_QTILES ? gb300::ATTN_ROWS_PER_ITEM : gb300::T1_ROWS;
+  p.n_qblocks = (Lq + rows - 1) / rows;
+  p.n_items = static_cast<int>(static_cast<long long>(B) * H * p.n_qblocks);
+  switch (schedule) {
+    case ATTN_SCHEDULE_ONE_QTILE:
+      return d == 64 ? launch_attn<64, ATTN_SCHEDULE_ONE_QTILE>(ds, mq, mk, mv, p, stream)
+                     : launch_attn<128, ATTN_SCHEDULE_ONE_QTILE>(ds, mq, mk, mv, p, stream);
+    case ATTN_SCHEDULE_SPLIT_KEYS:
+      return d == 64 ? launch_attn<64, ATTN_SCHEDULE_SPLIT_KEYS>(ds, mq, mk, mv, p, stream)
+                     : launch_attn<128, ATTN_SCHEDULE_SPLIT_KEYS>(ds, mq, mk, mv, p, stream);
+    default:
+      return d == 64 ? launch_attn<64, ATTN_SCHEDULE_TWO_QTILES>(ds, mq, mk, mv, p, stream)
+                     : launch_attn<128, ATTN_SCHEDULE_TWO_QTILES>(ds, mq, mk, mv, p, stream);
+  }
 }
 
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix, box cols_box x rows_box.
@@ -249,6 +272,14 @@ void attn_set_wait_limit_ns(uint64_t ns) {
   g_wait_limit_ns = ns ? static_cast<unsigned long long>(ns) : kDefaultWaitLimitNs;
 }
 
+attn_status_t attn_set_schedule(int schedule) {
+  if (schedule < ATTN_SCHEDULE_AUTO || schedule > ATTN_SCHEDULE_SPLIT_KEYS)
+    return ATTN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_schedule = schedule;
+  return ATTN_OK;
+}
+
 void attn_debug_skip_kv_load(long long index) {
   std::lock_guard<std::mutex> lock(g_mutex);
   g_debug_skip_kv_load = index < 0 ? -1 : index;
@@ -275,8 +306,8 @@ attn_status_t attn_fwd_gqa(const void* Q, const void* K, const void* V, int B, i
   if (!(scale == scale) || std::isinf(scale)) return ATTN_ERR_INVALID_ARG;
   if (d_k != d_v) return ATTN_ERR_UNSUPPORTED;
   if (d_k != 64 && d_k != 128) return ATTN_ERR_UNSUPPORTED;
-  const long long n_qblocks = (static_cast<long long>(Lq) + gb300::ATTN_ROWS_PER_ITEM - 1) /
-                              gb300::ATTN_ROWS_PER_ITEM;
+  // work items of the finer schedule (128 query rows each) must fit an int
+  const long long n_qblocks = (static_cast<long long>(Lq) + gb300::T1_ROWS - 1) / gb300::T1_ROWS;
   if (static_cast<long long>(B) * h * n_qblocks >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || h == 0 || Lq == 0) return ATTN_OK;
   if (!O) return ATTN_ERR_INVALID_ARG;
