@@ -72,6 +72,15 @@ def profiled_traffic(workload):
     return ent.get("dram_bytes_per_launch")
 
 
+def attention_kernel_name(B, H, Lq, d):
+    """The kernel the library's automatic schedule launches for this shape:
+    the split-keys kernel when B * H * ceil(Lq / 256) is below the SM count."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    split = B * H * ((Lq + 255) // 256) < sms
+    return ("attn_fwd_split_kernel<%d>" if split else "attn_fwd_kernel<%d>") % d
+
+
 def algorithmic_counts(w, kv_lens):
     """FLOPs, exponentials and HBM bytes of one pass (definitions in the design doc)."""
     flops = attn_flops(w.B, w.H, w.Lq, w.Lk, w.d_k, w.mask_kind, kv_lens)
@@ -337,7 +346,7 @@ def ours_arm(args, w):
         "unit": "TFLOP/s" if bound != "hbm" else "GB/s",
         "traffic": profiled_traffic(w.name),
         "peak_source": "%s (bf16 dense burst)" % peak_src if bound != "hbm" else peak_src,
-        "kernel": "attn_fwd_kernel<%d>" % w.d_k,
+        "kernel": attention_kernel_name(w.B, w.H, w.Lq, w.d_k),
         "roofline_time_ms": 1e3 * max(t_tensor, t_exp, t_hbm),
         "frac_of_roofline_time": 1e3 * max(t_tensor, t_exp, t_hbm) / ms,
         "exp_bound_fraction": t_exp / max(t_tensor, t_hbm),
@@ -472,7 +481,7 @@ def layer_arm(args, w):
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
                 "peak_source": "%s (bf16 dense burst)" % peak_src,
                 "kernel": {"qkv_gemm": "gemm_bf16_kernel", "wo_gemm": "gemm_bf16_kernel",
-                           "attention": "attn_fwd_kernel<%d>" % dk}[dom],
+                           "attention": attention_kernel_name(w.B, w.H, w.L, dk)}[dom],
                 "stages_ms": {k: v[1] for k, v in stages.items()},
                 "stages_tflops": {k: v[0] / (v[1] * 1e-3) / 1e12 for k, v in stages.items()}}
     cpu = None

@@ -227,23 +227,21 @@ void attn_set_wait_limit_ns(uint64_t ns);
  * Work schedules of the attention kernel.  Both compute the same function
  * (online softmax over 128-key tiles, fp32 accumulation, bf16 P); they differ
  * in how a CTA's work is laid out on the SM:
- *   ATTN_SCHEDULE_TWO_QTILES  256 query rows per work item, Q in shared
- *                             memory, one MMA issuer per 128-row tile
- *   ATTN_SCHEDULE_ONE_QTILE   128 query rows per work item, Q and P in tensor
- *                             memory, a double-buffered S, one issuer for
- *                             Q K^T and another for P V, two softmax threads
- *                             per query row
+ *   ATTN_SCHEDULE_TWO_QTILES  256 query rows per work item, two 128-row Q
+ *                             tiles with one softmax warpgroup and one MMA
+ *                             issuer warp each
  *   ATTN_SCHEDULE_SPLIT_KEYS  128 query rows per work item, its key tiles
  *                             dealt alternately to two softmax warpgroups
  *                             with separate accumulators, merged at the end
- *                             of the item; issuers as in ONE_QTILE
- *   ATTN_SCHEDULE_AUTO        the library picks one from the shape
+ *                             of the item; twice as many work items, for
+ *                             shapes with too few 256-row items to fill the GPU
+ *   ATTN_SCHEDULE_AUTO        SPLIT_KEYS when B * h * ceil(Lq / 256) is below
+ *                             the number of SMs, else TWO_QTILES (the default)
  */
 typedef enum {
   ATTN_SCHEDULE_AUTO = 0,
   ATTN_SCHEDULE_TWO_QTILES = 1,
-  ATTN_SCHEDULE_ONE_QTILE = 2,
-  ATTN_SCHEDULE_SPLIT_KEYS = 3
+  ATTN_SCHEDULE_SPLIT_KEYS = 2
 } attn_schedule_t;
 
 /*

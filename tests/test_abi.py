@@ -123,6 +123,6 @@ def test_schedule_selection(cdll):
     f = cdll.attn_set_schedule
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.c_int]
-    for s in (1, 2, 3, 0):     # two Q tiles, one Q tile, split keys, automatic
+    for s in (1, 2, 0):        # two Q tiles, split keys, automatic
         assert f(s) == 0
-    assert f(4) == 1 and f(-1) == 1
+    assert f(3) == 1 and f(-1) == 1

@@ -22,7 +22,7 @@ __all__ = [
     "attn_weights", "mha_layer_fwd",
     "mha_layer_workspace_bytes", "mha_layer_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gemm_bf16",
     "check_device_status", "set_wait_limit_ns", "set_schedule", "SCHEDULE_AUTO",
-    "SCHEDULE_TWO_QTILES", "SCHEDULE_ONE_QTILE", "SCHEDULE_SPLIT_KEYS", "debug_skip_kv_load", "library_path", "lib",
+    "SCHEDULE_TWO_QTILES", "SCHEDULE_SPLIT_KEYS", "debug_skip_kv_load", "library_path", "lib",
 ]
 
 MASK_NONE = 0
@@ -33,8 +33,7 @@ MASK_CAUSAL_BOTTOM_RIGHT = 4
 # attention work schedules (attn_schedule_t)
 SCHEDULE_AUTO = 0
 SCHEDULE_TWO_QTILES = 1
-SCHEDULE_ONE_QTILE = 2
-SCHEDULE_SPLIT_KEYS = 3
+SCHEDULE_SPLIT_KEYS = 2
 
 ATTN_OK = 0
 STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",

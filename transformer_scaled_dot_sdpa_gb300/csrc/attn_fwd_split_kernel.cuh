@@ -1,4 +1,4 @@
-// attn_fwd_t2_kernel.cuh -- attention forward, one 128-query tile per work
+// attn_fwd_split_kernel.cuh -- attention forward, one 128-query tile per work
 // item, its key tiles dealt alternately to two softmax warpgroups, for sm_103a.
 //
 // It computes the same thing as attn_fwd_kernel.cuh (online softmax of
@@ -34,13 +34,67 @@
 #include <cuda_bf16.h>
 
 #include "attn_fwd_kernel.cuh"
-#include "attn_fwd_t1_kernel.cuh"
 #include "ptx.cuh"
 
 namespace gb300 {
 
+constexpr int SPLIT_ROWS = 128;  // query rows per work item
+
+struct SplitItem {
+  int b, h, kvh, row0, nkv, kv_len, kv_len_raw;
+};
+
+// Item k of this CTA: one (b, h, 128-row query tile), heaviest first, dealt
+// in a boustrophedon order like attn_get_item.
+__device__ __forceinline__ bool split_get_item(const AttnParams& p, int k, SplitItem& it) {
+  const int G = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  const long long w = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
+  if (w >= p.n_items) return false;
+  const int BH = p.B * p.H;
+  const int rank = static_cast<int>(w / BH);
+  const int bh = static_cast<int>(w - static_cast<long long>(rank) * BH);
+  const int qt = p.n_qblocks - 1 - rank;
+  it.b = bh / p.H;
+  it.h = bh - it.b * p.H;
+  it.kvh = it.h / p.kv_group;
+  int kv_len = p.Lk;
+  it.kv_len_raw = p.Lk;
+  if (p.mask_kind & ATTN_MASK_PADDING_BIT) {
+    const int raw = p.kv_lens[it.b];
+    it.kv_len_raw = raw;
+    kv_len = raw < 0 ? 0 : (raw > p.Lk ? p.Lk : raw);
+  }
+  it.kv_len = kv_len;
+  it.row0 = qt * SPLIT_ROWS;
+  int n = 0;
+  const bool all_padded = (p.mask_kind & ATTN_MASK_PADDING_BIT) && it.row0 >= kv_len;
+  if (it.row0 < p.Lq && !all_padded) {
+    int lim = kv_len;
+    if (p.mask_kind & ATTN_MASK_CAUSAL_BIT) {
+      const int last = min(it.row0 + SPLIT_ROWS - 1, p.Lq - 1);
+      lim = min(lim, max(last + 1 + p.causal_offset, 0));
+    }
+    n = (lim + ATTN_BLOCK_N - 1) / ATTN_BLOCK_N;
+  }
+  it.nkv = n;
+  return true;
+}
+
+// Waits for the last load into each slot of a ring before the CTA exits (n
+// loads were issued in ring order; `skip` is a running index never loaded).
+__device__ __forceinline__ void split_drain_ring(uint64_t* full, int stages, uint32_t n,
+                                              long long skip, uint64_t limit_ns) {
+  for (int s = 0; s < stages; ++s) {
+    if (n <= static_cast<uint32_t>(s)) continue;
+    const uint32_t uses = (n - s + stages - 1) / stages;
+    const uint32_t last = s + (uses - 1u) * stages;
+    if (static_cast<long long>(last) != skip) mbar_wait_drain(&full[s], (uses - 1u) & 1u, limit_ns);
+  }
+}
+
 template <int D>
-struct T2Layout {
+struct SplitLayout {
   static constexpr int TILE_BYTES = 128 * D * 2;
   static constexpr int CHUNK_BYTES = 128 * 128;  // 128 rows x 64 bf16
   static constexpr int NCHUNK = D / 64;
@@ -74,16 +128,16 @@ struct T2Layout {
 // TMA producers
 // ---------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ void t2_qk_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+__device__ __forceinline__ void split_qk_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                                const AttnParams& p, uint8_t* smem,
                                                uint64_t* bars, const WaitCtl& ctl) {
-  using L = T2Layout<D>;
+  using L = SplitLayout<D>;
   tma_prefetch_desc(tmQ);
   tma_prefetch_desc(tmK);
   uint32_t q_loads = 0, kv_it = 0;
   bool ok = true;
-  T1Item it;
-  for (int k = 0; ok && t1_get_item(p, k, it); ++k) {
+  SplitItem it;
+  for (int k = 0; ok && split_get_item(p, k, it); ++k) {
     if (it.nkv == 0) continue;
     if (q_loads > 0) {
       // the previous item's S MMAs have read Q
@@ -111,18 +165,18 @@ __device__ __forceinline__ void t2_qk_producer(const CUtensorMap* tmQ, const CUt
   }
   // Unwind: every load this thread issued lands before the CTA exits.
   if (q_loads > 0) mbar_wait_drain(&bars[L::B_Q_FULL], (q_loads - 1u) & 1u, ctl.limit_ns);
-  t1_drain_ring(&bars[L::B_K_FULL], L::K_STAGES, kv_it, p.debug_skip_kv_load, ctl.limit_ns);
+  split_drain_ring(&bars[L::B_K_FULL], L::K_STAGES, kv_it, p.debug_skip_kv_load, ctl.limit_ns);
 }
 
 template <int D>
-__device__ __forceinline__ void t2_v_producer(const CUtensorMap* tmV, const AttnParams& p,
+__device__ __forceinline__ void split_v_producer(const CUtensorMap* tmV, const AttnParams& p,
                                               uint8_t* smem, uint64_t* bars, const WaitCtl& ctl) {
-  using L = T2Layout<D>;
+  using L = SplitLayout<D>;
   tma_prefetch_desc(tmV);
   uint32_t kv_it = 0;
   bool ok = true;
-  T1Item it;
-  for (int k = 0; ok && t1_get_item(p, k, it); ++k) {
+  SplitItem it;
+  for (int k = 0; ok && split_get_item(p, k, it); ++k) {
     for (int j = 0; j < it.nkv; ++j, ++kv_it) {
       const int s = static_cast<int>(kv_it % L::V_STAGES);
       const uint32_t reuse = kv_it / L::V_STAGES;
@@ -136,7 +190,7 @@ __device__ __forceinline__ void t2_v_producer(const CUtensorMap* tmV, const Attn
                        &bars[L::B_V_FULL + s], 64 * c, j * ATTN_BLOCK_N, it.kvh, it.b, p.packed);
     }
   }
-  t1_drain_ring(&bars[L::B_V_FULL], L::V_STAGES, kv_it, -1, ctl.limit_ns);
+  split_drain_ring(&bars[L::B_V_FULL], L::V_STAGES, kv_it, -1, ctl.limit_ns);
 }
 
 // ---------------------------------------------------------------------------
@@ -146,16 +200,16 @@ __device__ __forceinline__ void t2_v_producer(const CUtensorMap* tmV, const Attn
 // computed by all lanes stay warp-uniform, which keeps the issue of each
 // tcgen05.mma short.
 template <int D>
-__device__ __forceinline__ void t2_s_role(const AttnParams& p, uint8_t* smem, uint64_t* bars,
+__device__ __forceinline__ void split_s_role(const AttnParams& p, uint8_t* smem, uint64_t* bars,
                                           uint32_t tmem, const WaitCtl& ctl) {
-  using L = T2Layout<D>;
+  using L = SplitLayout<D>;
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, ATTN_BLOCK_N, false);
   const uint64_t q_desc = smem_desc_sw128(smem_u32(smem + L::Q_OFF), 16, 1024);
   const uint64_t k_desc = smem_desc_sw128(smem_u32(smem + L::K_OFF), 16, 1024);
   uint32_t t = 0, q_cnt = 0;  // running tile index, Q loads consumed
   bool ok = true;
-  T1Item it;
-  for (int k = 0; ok && t1_get_item(p, k, it); ++k) {
+  SplitItem it;
+  for (int k = 0; ok && split_get_item(p, k, it); ++k) {
     if (it.kv_len_raw != it.kv_len && elect_one()) atomicOr(p.status, ATTN_STATUS_BAD_KVLEN);
     if (it.nkv == 0) continue;
     ok = __all_sync(0xffffffffu, mbar_wait(&bars[L::B_Q_FULL], q_cnt & 1u, ctl));
@@ -200,15 +254,15 @@ __device__ __forceinline__ void t2_s_role(const AttnParams& p, uint8_t* smem, ui
 // P.V issuer (one warp): O_{t % 2} += P(t) V_t
 // ---------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ void t2_pv_role(const AttnParams& p, uint8_t* smem, uint64_t* bars,
+__device__ __forceinline__ void split_pv_role(const AttnParams& p, uint8_t* smem, uint64_t* bars,
                                            uint32_t tmem, const WaitCtl& ctl) {
-  using L = T2Layout<D>;
+  using L = SplitLayout<D>;
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);
   const uint64_t v_desc = smem_desc_sw128(smem_u32(smem + L::V_OFF), L::CHUNK_BYTES, 1024);
   uint32_t t = 0;
   bool ok = true;
-  T1Item it;
-  for (int k = 0; ok && t1_get_item(p, k, it); ++k) {
+  SplitItem it;
+  for (int k = 0; ok && split_get_item(p, k, it); ++k) {
     for (int j = 0; j < it.nkv; ++j, ++t) {
       const int s = static_cast<int>(t % L::V_STAGES);
       ok = __all_sync(0xffffffffu, mbar_wait(&bars[L::B_V_FULL + s], (t / L::V_STAGES) & 1u, ctl));
@@ -241,10 +295,10 @@ __device__ __forceinline__ void t2_pv_role(const AttnParams& p, uint8_t* smem, u
 // softmax / correction / epilogue: warpgroup g, one thread per query row
 // ---------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ void t2_softmax_role(const int g, const AttnParams& p, uint8_t* smem,
+__device__ __forceinline__ void split_softmax_role(const int g, const AttnParams& p, uint8_t* smem,
                                                 uint64_t* bars, uint32_t tmem,
                                                 const WaitCtl& ctl) {
-  using L = T2Layout<D>;
+  using L = SplitLayout<D>;
   constexpr int DH = D / 2;  // output columns written by each group
   const int rloc = static_cast<int>(threadIdx.x & 127u);
   const int q = (rloc >> 5);
@@ -260,8 +314,8 @@ __device__ __forceinline__ void t2_softmax_role(const int g, const AttnParams& p
   uint32_t t0 = 0;     // running index of the item's first tile
   uint32_t x_cnt = 0;  // exchanges with the other group
   bool ok = true;
-  T1Item it;
-  for (int k = 0; ok && t1_get_item(p, k, it); ++k) {
+  SplitItem it;
+  for (int k = 0; ok && split_get_item(p, k, it); ++k) {
     if (it.row0 >= p.Lq) continue;
     const int r = it.row0 + rloc;
     const int nkv = it.nkv;
@@ -487,10 +541,10 @@ __device__ __forceinline__ void t2_softmax_role(const int g, const AttnParams& p
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(ATTN_THREADS, 1)
-    attn_fwd_t2_kernel(const __grid_constant__ CUtensorMap tmQ,
+    attn_fwd_split_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  using L = T2Layout<D>;
+  using L = SplitLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~static_cast<uintptr_t>(1023u));
@@ -536,17 +590,17 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   if (warp >= 8) {
     reg_dealloc<ATTN_REGS_CONTROL>();
     if (warp == 8) {
-      t2_s_role<D>(p, smem, bars, tmem, ctl);
+      split_s_role<D>(p, smem, bars, tmem, ctl);
     } else if (warp == 9) {
-      if (lane == 0) t2_qk_producer<D>(&tmQ, &tmK, p, smem, bars, ctl);
+      if (lane == 0) split_qk_producer<D>(&tmQ, &tmK, p, smem, bars, ctl);
     } else if (warp == 10) {
-      t2_pv_role<D>(p, smem, bars, tmem, ctl);
+      split_pv_role<D>(p, smem, bars, tmem, ctl);
     } else {
-      if (lane == 0) t2_v_producer<D>(&tmV, p, smem, bars, ctl);
+      if (lane == 0) split_v_producer<D>(&tmV, p, smem, bars, ctl);
     }
   } else {
     reg_alloc<ATTN_REGS_SOFTMAX>();
-    t2_softmax_role<D>(warp >> 2, p, smem, bars, tmem, ctl);
+    split_softmax_role<D>(warp >> 2, p, smem, bars, tmem, ctl);
   }
 
   tc_fence_before();

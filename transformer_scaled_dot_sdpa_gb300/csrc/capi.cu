@@ -11,8 +11,7 @@
 
 #include "../../include/gb300attn.h"
 #include "attn_fwd_kernel.cuh"
-#include "attn_fwd_t1_kernel.cuh"
-#include "attn_fwd_t2_kernel.cuh"
+#include "attn_fwd_split_kernel.cuh"
 #include "attn_weights_kernel.cuh"
 #include "gemm_kernel.cuh"
 
@@ -35,7 +34,7 @@ struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   unsigned int* status = nullptr;
-  bool attn_attr[6] = {false, false, false, false, false, false};
+  bool attn_attr[4] = {false, false, false, false};
   bool gemm_attr = false;
   void* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch
 };
@@ -126,14 +125,11 @@ template <int D, int SCHEDULE>
 attn_status_t launch_attn(DeviceState* ds, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, const gb300::AttnParams& p,
                           cudaStream_t stream) {
-  const int attr_idx = (D == 64 ? 0 : 1) + 2 * (SCHEDULE - 1);
-  const int smem = SCHEDULE == ATTN_SCHEDULE_ONE_QTILE    ? gb300::T1Layout<D>::SMEM_BYTES
-                   : SCHEDULE == ATTN_SCHEDULE_SPLIT_KEYS ? gb300::T2Layout<D>::SMEM_BYTES
-                                                          : gb300::AttnLayout<D>::SMEM_BYTES;
+  constexpr bool split = SCHEDULE == ATTN_SCHEDULE_SPLIT_KEYS;
+  const int attr_idx = (D == 64 ? 0 : 1) + (split ? 2 : 0);
+  const int smem = split ? gb300::SplitLayout<D>::SMEM_BYTES : gb300::AttnLayout<D>::SMEM_BYTES;
   void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, gb300::AttnParams) =
-      SCHEDULE == ATTN_SCHEDULE_ONE_QTILE    ? gb300::attn_fwd_t1_kernel<D>
-      : SCHEDULE == ATTN_SCHEDULE_SPLIT_KEYS ? gb300::attn_fwd_t2_kernel<D>
-                                             : gb300::attn_fwd_kernel<D>;
+      split ? gb300::attn_fwd_split_kernel<D> : gb300::attn_fwd_kernel<D>;
   if (!ds->attn_attr[attr_idx]) {
     // The kernels hand registers between warpgroups (setmaxnreg); the split
     // adds up to exactly ATTN_THREADS x ATTN_REGS_AT_LAUNCH, so a build with a
@@ -186,21 +182,23 @@ attn_status_t run_attention(DeviceState* ds, const CUtensorMap& mq, const CUtens
     p.debug_skip_kv_load = g_debug_skip_kv_load;
     schedule = g_schedule;
   }
-  if (schedule == ATTN_SCHEDULE_AUTO) schedule = ATTN_SCHEDULE_TWO_QTILES;
-  const int rows = schedule == ATTN_SCHEDULE_TWO_QTILES ? gb300::ATTN_ROWS_PER_ITEM : gb300::T1_ROWS;
+  if (schedule == ATTN_SCHEDULE_AUTO) {
+    // Too few 256-row items to give every SM one: take the schedule with
+    // 128-row items, which has twice as many (measured: 1.6-1.7x faster on
+    // causal 1x8x4096 and 1x4x8192 at d = 128, slower from 256 items up).
+    const long long items_two = static_cast<long long>(B) * H *
+                                ((Lq + gb300::ATTN_ROWS_PER_ITEM - 1) / gb300::ATTN_ROWS_PER_ITEM);
+    schedule = items_two < ds->num_sms ? ATTN_SCHEDULE_SPLIT_KEYS : ATTN_SCHEDULE_TWO_QTILES;
+  }
+  const bool split = schedule == ATTN_SCHEDULE_SPLIT_KEYS;
+  const int rows = split ? gb300::SPLIT_ROWS : gb300::ATTN_ROWS_PER_ITEM;
   p.n_qblocks = (Lq + rows - 1) / rows;
   p.n_items = static_cast<int>(static_cast<long long>(B) * H * p.n_qblocks);
-  switch (schedule) {
-    case ATTN_SCHEDULE_ONE_QTILE:
-      return d == 64 ? launch_attn<64, ATTN_SCHEDULE_ONE_QTILE>(ds, mq, mk, mv, p, stream)
-                     : launch_attn<128, ATTN_SCHEDULE_ONE_QTILE>(ds, mq, mk, mv, p, stream);
-    case ATTN_SCHEDULE_SPLIT_KEYS:
-      return d == 64 ? launch_attn<64, ATTN_SCHEDULE_SPLIT_KEYS>(ds, mq, mk, mv, p, stream)
-                     : launch_attn<128, ATTN_SCHEDULE_SPLIT_KEYS>(ds, mq, mk, mv, p, stream);
-    default:
-      return d == 64 ? launch_attn<64, ATTN_SCHEDULE_TWO_QTILES>(ds, mq, mk, mv, p, stream)
-                     : launch_attn<128, ATTN_SCHEDULE_TWO_QTILES>(ds, mq, mk, mv, p, stream);
-  }
+  if (split)
+    return d == 64 ? launch_attn<64, ATTN_SCHEDULE_SPLIT_KEYS>(ds, mq, mk, mv, p, stream)
+                   : launch_attn<128, ATTN_SCHEDULE_SPLIT_KEYS>(ds, mq, mk, mv, p, stream);
+  return d == 64 ? launch_attn<64, ATTN_SCHEDULE_TWO_QTILES>(ds, mq, mk, mv, p, stream)
+                 : launch_attn<128, ATTN_SCHEDULE_TWO_QTILES>(ds, mq, mk, mv, p, stream);
 }
 
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix, box cols_box x rows_box.
@@ -307,7 +305,7 @@ attn_status_t attn_fwd_gqa(const void* Q, const void* K, const void* V, int B, i
   if (d_k != d_v) return ATTN_ERR_UNSUPPORTED;
   if (d_k != 64 && d_k != 128) return ATTN_ERR_UNSUPPORTED;
   // work items of the finer schedule (128 query rows each) must fit an int
-  const long long n_qblocks = (static_cast<long long>(Lq) + gb300::T1_ROWS - 1) / gb300::T1_ROWS;
+  const long long n_qblocks = (static_cast<long long>(Lq) + gb300::SPLIT_ROWS - 1) / gb300::SPLIT_ROWS;
   if (static_cast<long long>(B) * h * n_qblocks >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || h == 0 || Lq == 0) return ATTN_OK;
   if (!O) return ATTN_ERR_INVALID_ARG;

@@ -207,13 +207,6 @@ __device__ __forceinline__ bool elect_one() {
   return e != 0u;
 }
 
-// Shared memory -> TMEM copy of a 128-row x 256-bit block (one row per lane,
-// 8 columns), the source described like an MMA operand.  Asynchronous; it is
-// ordered before later tcgen05.mma of the same thread, and a commit tracks it.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
