@@ -158,6 +158,47 @@ def max_over_ranks(x, world, device="cuda"):
     return float(t.item())
 
 
+def l2_bytes(dev):
+    import torch
+    p = torch.cuda.get_device_properties(dev)
+    return int(getattr(p, "L2_cache_size", 0) or (128 << 20))
+
+
+def l2_flush_buffer(input_bytes, dev):
+    """A buffer of twice the L2 size when a step's inputs fit in L2 (their
+    timed calls then start from a cold L2), else None."""
+    import torch
+    l2 = l2_bytes(dev)
+    if input_bytes > l2:
+        return None
+    return torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+
+def time_calls(fn, n, stream, dev, flush=None):
+    """Mean ms per call of fn over n calls, CUDA events on `stream`.  With a
+    flush buffer each call is timed on its own and the buffer is rewritten
+    between calls, outside the events."""
+    import torch
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / n
+    evs = []
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize(dev)
+    return sum(a.elapsed_time(b) for a, b in evs) / n
+
+
 def replica_workload(w, rank):
     """Rank r's replica: the same shapes, an independent seed (weak scaling;
     attention of distinct sequences needs no exchange between ranks)."""
@@ -237,12 +278,18 @@ def reference_arm(args, w):
     return 0
 
 
-def workload_config(w, world):
+def attn_input_bytes(w):
+    return 2 * w.B * w.H * (w.Lq + 2 * w.Lk) * w.d_k
+
+
+def workload_config(w, world, flushed=False):
     mask = {0: "none", 1: "causal", 2: "padding", 3: "causal+padding"}[w.mask_kind]
+    mb = attn_input_bytes(w) / 1e6
+    l2 = ("Q/K/V %.1f MB fit in L2: L2 flushed (a 2x L2 buffer rewritten) before every timed "
+          "call, outside its events" % mb if flushed else
+          "inputs larger than L2 (Q/K/V %.0f MB), no flush" % mb)
     return {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d_k,
-            "mask": mask, "parallelism": "replicas x%d" % world,
-            "l2": "inputs larger than L2 (Q/K/V %.0f MB), no flush" %
-                  (2.0 * w.B * w.H * (w.Lq + 2 * w.Lk) * w.d_k / 1e6)}
+            "mask": mask, "parallelism": "replicas x%d" % world, "l2": l2}
 
 
 # ---------------------------------------------------------------------------
@@ -283,22 +330,20 @@ def ours_arm(args, w):
         step()
     g.check_device_status(stream)
 
+    flush = l2_flush_buffer(attn_input_bytes(w), dev)
     clocks = ClockSampler(dev.index if world == 1 else local)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize(dev)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
+    ms = time_calls(step, args.steps, stream, dev, flush)
     barrier(world)
     clk = clocks.stop()
     g.check_device_status(stream)
-    ms = ev0.elapsed_time(ev1) / args.steps
     ms_max = max_over_ranks(ms, world)
+    warm_ms = None
+    if flush is not None:  # the same calls back to back, inputs warm in L2
+        warm_ms = max_over_ranks(time_calls(step, args.steps, stream, dev), world)
+        g.check_device_status(stream)
 
     # end to end through the public API with host buffers: pinned H2D of the
     # inputs, the attention call, D2H of O and LSE, every step
@@ -364,7 +409,7 @@ def ours_arm(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(w, world),
+        "config": workload_config(w, world, flushed=flush is not None),
         "e2e": {"value": e2e_value, "unit": UNIT,
                 "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
                 "d2h_bytes_per_step": int(hO.numel() * 2 + hL.numel() * 4),
@@ -374,6 +419,9 @@ def ours_arm(args, w):
         "cpu_baseline": cpu,
         "clocks": clk,
     }
+    if warm_ms is not None:
+        line["config"]["warm_l2"] = {"value": world * flops / (warm_ms * 1e-3) / 1e12,
+                                     "unit": UNIT, "ms_per_step": warm_ms}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -435,10 +483,14 @@ def layer_arm(args, w):
     for _ in range(args.warmup):
         step()
     g.check_device_status(stream)
+    # X and the weights (the step's inputs) fit in L2: flush it before every
+    # timed call
+    flush = l2_flush_buffer(2 * (x.numel() + wqkv.numel() + wo.numel()), dev)
     clocks = ClockSampler(dev.index if world == 1 else local)
     clocks.start()
     barrier(world)
-    ms = timed(step, args.steps)
+    torch.cuda.synchronize(dev)
+    ms = time_calls(step, args.steps, stream, dev, flush)
     barrier(world)
     clk = clocks.stop()
     g.check_device_status(stream)
@@ -449,13 +501,16 @@ def layer_arm(args, w):
     qkv = torch.empty((N, 3 * dm), dtype=torch.bfloat16, device=dev)
     cat = torch.empty((N, dm), dtype=torch.bfloat16, device=dev)
     x2 = x.view(N, dm)
-    ms_qkv = timed(lambda: g.gemm_bf16(x2, wqkv, out=qkv, stream=stream), args.steps)
-    ms_wo = timed(lambda: g.gemm_bf16(cat, wo, out=y.view(N, dm), stream=stream), args.steps)
+    ms_qkv = time_calls(lambda: g.gemm_bf16(x2, wqkv, out=qkv, stream=stream), args.steps, stream,
+                        dev, flush)
+    ms_wo = time_calls(lambda: g.gemm_bf16(cat, wo, out=y.view(N, dm), stream=stream), args.steps,
+                       stream, dev, flush)
     qh = torch.empty((w.B, w.H, w.L, dk), dtype=torch.bfloat16, device=dev).normal_()
     kh, vh = torch.empty_like(qh).normal_(), torch.empty_like(qh).normal_()
     oh = torch.empty_like(qh)
-    ms_att = timed(lambda: g.attn_fwd(qh, kh, vh, mask_kind=w.mask_kind, scale=w.scale, out=oh,
-                                      return_lse=False, stream=stream), args.steps)
+    ms_att = time_calls(lambda: g.attn_fwd(qh, kh, vh, mask_kind=w.mask_kind, scale=w.scale,
+                                           out=oh, return_lse=False, stream=stream),
+                        args.steps, stream, dev, flush)
     g.check_device_status(stream)
 
     # end to end: X in from pinned host memory, Y back, every step
@@ -507,7 +562,10 @@ def layer_arm(args, w):
         "config": {"workload": w.name, "B": w.B, "L": w.L, "d_model": dm, "H": w.H,
                    "mask": "causal" if w.mask_kind & MASK_CAUSAL else "none",
                    "parallelism": "replicas x%d" % world,
-                   "l2": "no flush; X 34 MB, QKV workspace 101 MB, weights 8 MB"},
+                   "l2": ("X and weights %.0f MB fit in L2: L2 flushed (a 2x L2 buffer "
+                          "rewritten) before every timed call, outside its events"
+                          % (2e-6 * (x.numel() + wqkv.numel() + wo.numel()))
+                          if flush is not None else "inputs larger than L2, no flush")},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(hx.numel() * 2), "d2h_bytes_per_step": int(hy.numel() * 2),
                 "steps": e2e_steps, "ms_per_step": e2e_ms},

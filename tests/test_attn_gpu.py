@@ -141,6 +141,44 @@ def test_large_workloads_sampled(cuda_lib, name, rows_per_head):
     assert np.array_equal(O[:, :, 0, :], bf16_to_f32(inp["v"][:, :, 0, :]))
 
 
+_ORACLE_CACHE = {}
+
+
+def _oracle_rows(name, rows):
+    """Oracle O and LSE of a workload on the given flat rows (cached: the
+    module runs once per kernel schedule, the oracle answer is the same)."""
+    key = (name, rows.tobytes() if rows is not None else None)
+    if key not in _ORACLE_CACHE:
+        w = WORKLOADS[name]
+        inp = make_workload_inputs(w)
+        _ORACLE_CACHE.clear()
+        _ORACLE_CACHE[key] = oracle.attention(inp["q"], inp["k"], inp["v"], mask_kind=w.mask_kind,
+                                              scale=w.scale, rows=rows)
+    return _ORACLE_CACHE[key]
+
+
+def test_causal_l4096_every_row(cuda_lib):
+    """Every query row of the causal B=4, h=16, L=4096, d=128 workload, in the
+    launch configuration the benchmark times, against the oracle."""
+    name = "mha_causal_b4_h16_l4096_d128"
+    w = WORKLOADS[name]
+    O, L = _run(cuda_lib, make_workload_inputs(w), w.mask_kind, scale=w.scale)
+    Or, Lr = _oracle_rows(name, None)
+    compare_attention(O, L, Or, Lr, name)
+
+
+def test_long_context_two_whole_heads(cuda_lib):
+    """Two complete heads (the first and the last) of the causal B=1, h=32,
+    L=32768, d=128 workload: every query row, every key."""
+    name = "mha_causal_longctx_b1_h32_l32768_d128"
+    w = WORKLOADS[name]
+    O, L = _run(cuda_lib, make_workload_inputs(w), w.mask_kind, scale=w.scale)
+    heads = [0, w.B * w.H - 1]
+    rows = np.concatenate([bh * w.Lq + np.arange(w.Lq, dtype=np.int64) for bh in heads])
+    Or, Lr = _oracle_rows(name, rows)
+    compare_attention(O.reshape(-1, w.d_v)[rows], L.reshape(-1)[rows], Or, Lr, name + " heads 0, 31")
+
+
 MASK_BR = 4  # causal, aligned to the last key
 
 GQA = [(2, 8, 8, 300, 300, 128), (1, 8, 2, 257, 257, 64), (2, 6, 1, 200, 200, 128),
