@@ -112,6 +112,40 @@ attn_status_t attn_fwd_gqa(const void* Q, const void* K, const void* V, int B, i
                            void* stream);
 
 /*
+ * attn_decode -- attn_fwd_gqa for few query rows against a long key/value
+ * cache (decoding: the Lq new tokens are the last Lq of each sequence, so the
+ * usual mask is ATTN_MASK_CAUSAL_BOTTOM_RIGHT, with kv_lens for caches of
+ * different lengths).  It computes exactly what attn_fwd_gqa computes.
+ *
+ * How it differs: work is split over the keys.  Each (b, K/V head, chunk of
+ * keys) is one work item whose Q tile holds the Lq rows of all h/h_kv query
+ * heads that share the K/V head, so every key/value row is read once per K/V
+ * head; a second kernel merges the chunks' partial softmaxes by the online
+ * softmax identity ("Self-Attention 机制", section "Softmax 的数值稳定性与
+ * Online Softmax").
+ *
+ *   Arguments as for attn_fwd_gqa with d = d_k = d_v, plus
+ *   workspace   device scratch of at least attn_decode_workspace_bytes(...)
+ *               bytes, 256-byte aligned, owned by the caller; not read
+ *               before it is written.  Calls that share it must not overlap.
+ *
+ * Supported: d in {64, 128}; (h / h_kv) * Lq <= 128 (else
+ * ATTN_ERR_UNSUPPORTED: use attn_fwd_gqa).  A workspace smaller than needed
+ * returns ATTN_ERR_INVALID_ARG.  Other errors as for attn_fwd_gqa.
+ */
+attn_status_t attn_decode(const void* Q, const void* K, const void* V, int B, int h, int h_kv,
+                          int Lq, int Lk, int d, int mask_kind, const int32_t* kv_lens,
+                          float scale, void* O, float* LSE, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/*
+ * attn_decode_workspace_bytes -- scratch size attn_decode needs for these
+ * sizes on the current device (it depends on the device's SM count); 0 for
+ * empty or unsupported sizes.
+ */
+size_t attn_decode_workspace_bytes(int B, int h, int h_kv, int Lq, int Lk, int d);
+
+/*
  * attn_weights -- the attention matrix A for inspection of small problems.
  * The pages' reference snippets return A = softmax(Q K^T / sqrt(d_k) + M) next
  * to the output ("attention-mechanism" page, section "最小实现";

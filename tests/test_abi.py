@@ -126,3 +126,21 @@ def test_schedule_selection(cdll):
     for s in (1, 2, 0):        # two Q tiles, split keys, automatic
         assert f(s) == 0
     assert f(3) == 1 and f(-1) == 1
+
+
+def test_decode_validation(cdll):
+    f = cdll.attn_decode
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    f.restype = i
+    f.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, ctypes.c_float, vp, vp, vp, sz, vp]
+    p = ctypes.c_void_p(0x1000)
+    INVALID, UNSUPPORTED, MISALIGNED = 1, 2, 3
+    assert f(p, p, p, 1, 8, 3, 1, 64, 128, 4, None, 0.0, p, None, p, 1 << 20, None) == INVALID
+    assert f(p, p, p, 1, 8, 2, 1, 64, 128, 5, None, 0.0, p, None, p, 1 << 20, None) == INVALID
+    assert f(p, p, p, 1, 8, 2, 1, 64, 96, 4, None, 0.0, p, None, p, 1 << 20, None) == UNSUPPORTED
+    # 8 query heads per K/V head x 17 rows > one 128-row tile
+    assert f(p, p, p, 1, 8, 1, 17, 64, 128, 4, None, 0.0, p, None, p, 1 << 20, None) == UNSUPPORTED
+    assert f(p, p, p, 1, 8, 2, 1, 64, 128, 4, None, 0.0, p, None, None, 0, None) == INVALID
+    bad = ctypes.c_void_p(0x1080)  # 16-byte but not 256-byte aligned workspace
+    assert f(p, p, p, 1, 8, 2, 1, 64, 128, 4, None, 0.0, p, None, bad, 1 << 20, None) == MISALIGNED
+    assert f(None, None, None, 0, 8, 2, 1, 64, 128, 4, None, 0.0, None, None, None, 0, None) == 0

@@ -19,6 +19,7 @@ import torch
 
 __all__ = [
     "MASK_NONE", "MASK_CAUSAL", "MASK_PADDING", "MASK_CAUSAL_BOTTOM_RIGHT", "AttnError", "attn_fwd",
+    "attn_decode", "attn_decode_workspace_bytes",
     "attn_weights", "mha_layer_fwd",
     "mha_layer_workspace_bytes", "mha_layer_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gemm_bf16",
     "check_device_status", "set_wait_limit_ns", "set_schedule", "SCHEDULE_AUTO",
@@ -67,6 +68,11 @@ def _load():
     L.attn_fwd_gqa.restype = i32
     L.attn_fwd_gqa.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp,
                                vp, vp]
+    L.attn_decode.restype = i32
+    L.attn_decode.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp, vp, sz,
+                              vp]
+    L.attn_decode_workspace_bytes.restype = sz
+    L.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     L.attn_weights.restype = i32
     L.attn_weights.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp]
     L.mha_layer_workspace_bytes.restype = sz
@@ -153,6 +159,44 @@ def attn_fwd(q, k, v, mask_kind=MASK_NONE, kv_lens=None, scale=None, out=None, l
                               int(mask_kind), _ptr(kv_lens), float(scale) if scale else 0.0,
                               _ptr(out), _ptr(lse), _stream_handle(stream))
         _check(st, "attn_fwd_gqa")
+    return out, lse
+
+
+def attn_decode_workspace_bytes(B, h, h_kv, Lq, Lk, d):
+    return int(lib.attn_decode_workspace_bytes(B, h, h_kv, Lq, Lk, d))
+
+
+def attn_decode(q, k, v, mask_kind=MASK_CAUSAL_BOTTOM_RIGHT, kv_lens=None, scale=None, out=None,
+                lse=None, return_lse=True, workspace=None, stream=None):
+    """attn_fwd for few query rows against a long K/V cache, split over the
+    keys (the query rows of the heads sharing a K/V head in one tile).  Same
+    arguments and results as attn_fwd; (h // h_kv) * Lq <= 128.  ``workspace``
+    (uint8 CUDA tensor) is allocated when not given."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dev_tensor(t, n, torch.bfloat16)
+    B, h, Lq, d = q.shape
+    h_kv, Lk = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, h_kv, Lk, d) or tuple(v.shape) != (B, h_kv, Lk, d):
+        raise ValueError("q/k/v shapes do not match")
+    if out is None:
+        out = torch.empty((B, h, Lq, d), dtype=torch.bfloat16, device=q.device)
+    _dev_tensor(out, "out", torch.bfloat16)
+    if tuple(out.shape) != (B, h, Lq, d):
+        raise ValueError("out has the wrong shape")
+    if lse is None and return_lse:
+        lse = torch.empty((B, h, Lq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _dev_tensor(lse, "lse", torch.float32)
+    if kv_lens is not None:
+        _dev_tensor(kv_lens, "kv_lens", torch.int32)
+    need = attn_decode_workspace_bytes(B, h, h_kv, Lq, Lk, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _dev_tensor(workspace, "workspace", torch.uint8)
+    st = lib.attn_decode(_ptr(q), _ptr(k), _ptr(v), B, h, h_kv, Lq, Lk, d, int(mask_kind),
+                         _ptr(kv_lens), float(scale) if scale else 0.0, _ptr(out), _ptr(lse),
+                         _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(st, "attn_decode")
     return out, lse
 
 

@@ -42,15 +42,48 @@ constexpr int SPLIT_ROWS = 128;  // query rows per work item
 
 struct SplitItem {
   int b, h, kvh, row0, nkv, kv_len, kv_len_raw;
+  int k0;     // first key of the item's key range
+  int chunk;  // decode: chunk index; qrow: flat index of the first packed Q row
+  int qrow;
 };
 
-// Item k of this CTA: one (b, h, 128-row query tile), heaviest first, dealt
-// in a boustrophedon order like attn_get_item.
+// Item k of this CTA, dealt in a boustrophedon order like attn_get_item.
+// Attention: one (b, h, 128-row query tile), heaviest first.  Decode: one
+// (b, K/V head, key chunk), chunk-major.
 __device__ __forceinline__ bool split_get_item(const AttnParams& p, int k, SplitItem& it) {
   const int G = static_cast<int>(gridDim.x);
   const int c = static_cast<int>(blockIdx.x);
   const long long w = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
   if (w >= p.n_items) return false;
+  if (p.decode) {
+    const int hkv = p.H / p.kv_group;
+    const int pairs = p.B * hkv;
+    it.chunk = static_cast<int>(w / pairs);
+    const int bk = static_cast<int>(w - static_cast<long long>(it.chunk) * pairs);
+    it.b = bk / hkv;
+    it.kvh = bk - it.b * hkv;
+    it.h = it.kvh * p.kv_group;
+    it.qrow = (it.b * p.H + it.h) * p.Lq;
+    int kv_len = p.Lk;
+    it.kv_len_raw = p.Lk;
+    if (p.mask_kind & ATTN_MASK_PADDING_BIT) {
+      const int raw = p.kv_lens[it.b];
+      it.kv_len_raw = raw;
+      kv_len = raw < 0 ? 0 : (raw > p.Lk ? p.Lk : raw);
+    }
+    it.kv_len = kv_len;
+    it.row0 = 0;
+    it.k0 = it.chunk * p.kv_chunk;
+    // keys the last query row may see bound those of every row of the item
+    int lim = kv_len;
+    if (p.mask_kind & ATTN_MASK_CAUSAL_BIT) lim = min(lim, max(p.Lq + p.causal_offset, 0));
+    const int hi = min(lim, it.k0 + p.kv_chunk);
+    it.nkv = hi > it.k0 ? (hi - it.k0 + ATTN_BLOCK_N - 1) / ATTN_BLOCK_N : 0;
+    return true;
+  }
+  it.k0 = 0;
+  it.chunk = 0;
+  it.qrow = 0;
   const int BH = p.B * p.H;
   const int rank = static_cast<int>(w / BH);
   const int bh = static_cast<int>(w - static_cast<long long>(rank) * BH);
@@ -145,9 +178,14 @@ __device__ __forceinline__ void split_qk_producer(const CUtensorMap* tmQ, const 
       if (!ok) break;
     }
     mbar_arrive_expect_tx(&bars[L::B_Q_FULL], L::TILE_BYTES);
-    for (int c = 0; c < L::NCHUNK; ++c)
-      attn_load_tile(tmQ, smem + L::Q_OFF + c * L::CHUNK_BYTES, &bars[L::B_Q_FULL], 64 * c,
-                     it.row0, it.h, it.b, p.packed);
+    for (int c = 0; c < L::NCHUNK; ++c) {
+      if (p.decode)  // 2-D map over the [B*H*Lq, D] query rows
+        tma_load_2d(smem + L::Q_OFF + c * L::CHUNK_BYTES, tmQ, &bars[L::B_Q_FULL], 64 * c,
+                    it.qrow);
+      else
+        attn_load_tile(tmQ, smem + L::Q_OFF + c * L::CHUNK_BYTES, &bars[L::B_Q_FULL], 64 * c,
+                       it.row0, it.h, it.b, p.packed);
+    }
     ++q_loads;
     for (int j = 0; j < it.nkv; ++j, ++kv_it) {
       const int s = static_cast<int>(kv_it % L::K_STAGES);
@@ -160,7 +198,8 @@ __device__ __forceinline__ void split_qk_producer(const CUtensorMap* tmQ, const 
       mbar_arrive_expect_tx(&bars[L::B_K_FULL + s], L::TILE_BYTES);
       for (int c = 0; c < L::NCHUNK; ++c)
         attn_load_tile(tmK, smem + L::K_OFF + s * L::TILE_BYTES + c * L::CHUNK_BYTES,
-                       &bars[L::B_K_FULL + s], 64 * c, j * ATTN_BLOCK_N, it.kvh, it.b, p.packed);
+                       &bars[L::B_K_FULL + s], 64 * c, it.k0 + j * ATTN_BLOCK_N, it.kvh, it.b,
+                       p.packed);
     }
   }
   // Unwind: every load this thread issued lands before the CTA exits.
@@ -187,7 +226,8 @@ __device__ __forceinline__ void split_v_producer(const CUtensorMap* tmV, const A
       mbar_arrive_expect_tx(&bars[L::B_V_FULL + s], L::TILE_BYTES);
       for (int c = 0; c < L::NCHUNK; ++c)
         attn_load_tile(tmV, smem + L::V_OFF + s * L::TILE_BYTES + c * L::CHUNK_BYTES,
-                       &bars[L::B_V_FULL + s], 64 * c, j * ATTN_BLOCK_N, it.kvh, it.b, p.packed);
+                       &bars[L::B_V_FULL + s], 64 * c, it.k0 + j * ATTN_BLOCK_N, it.kvh, it.b,
+                       p.packed);
     }
   }
   split_drain_ring(&bars[L::B_V_FULL], L::V_STAGES, kv_it, -1, ctl.limit_ns);
@@ -317,7 +357,10 @@ __device__ __forceinline__ void split_softmax_role(const int g, const AttnParams
   SplitItem it;
   for (int k = 0; ok && split_get_item(p, k, it); ++k) {
     if (it.row0 >= p.Lq) continue;
-    const int r = it.row0 + rloc;
+    // query index of this thread's row: the tile's rows, or in decode the
+    // packed (head, query) rows, of which the first q_rows are live
+    const int r = p.decode ? rloc % p.Lq : it.row0 + rloc;
+    const bool live_row = p.decode ? rloc < p.q_rows : r < p.Lq;
     const int nkv = it.nkv;
     int limit = it.kv_len;  // this row attends to keys [0, limit)
     if (causal) limit = min(limit, max(r + 1 + p.causal_offset, 0));
@@ -350,7 +393,7 @@ __device__ __forceinline__ void split_softmax_role(const int g, const AttnParams
         s[64 + i] = __uint_as_float(rc[i]);
         s[96 + i] = __uint_as_float(rd[i]);
       }
-      const int nvalid = limit - j * ATTN_BLOCK_N;
+      const int nvalid = limit - (it.k0 + j * ATTN_BLOCK_N);
       if (nvalid < ATTN_BLOCK_N) {
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = (i < nvalid) ? s[i] : -INFINITY;
@@ -476,15 +519,19 @@ __device__ __forceinline__ void split_softmax_role(const int g, const AttnParams
     const float w_oth = (cnt_o > 0 && mo != -INFINITY) ? ex2_approx(mo - mm) : 0.f;
     const float lsum = w_own * l + w_oth * lo;
     const float lbsum = w_own * lb + w_oth * lbo;
-    const bool in_range = r < p.Lq;
-    const bool zero_row = padded_row || nkv == 0 || limit <= 0 || !(lbsum > 0.f);
-    const float inv_l = zero_row ? 0.f : 1.0f / lbsum;
+    const bool in_range = live_row;
+    const bool zero_row = padded_row || nkv == 0 || limit <= it.k0 || !(lbsum > 0.f);
+    // decode writes the chunk's partial unnormalised (the chunks are merged
+    // by attn_decode_combine_kernel); attention divides by the row sum
+    const float inv_l = zero_row ? 0.f : (p.decode ? 1.0f : 1.0f / lbsum);
     const float f0 = (g == 0 ? w_own : w_oth) * inv_l;  // weight of O_0
     const float f1 = (g == 0 ? w_oth : w_own) * inv_l;  // weight of O_1
     const bool has0 = (g == 0 ? cnt : cnt_o) > 0;
     const bool has1 = (g == 0 ? cnt_o : cnt) > 0;
-    __nv_bfloat16* orow = p.O + it.b * p.o_stride_b + it.h * p.o_stride_h +
-                          static_cast<long long>(r) * p.o_stride_l + DH * g;
+    const long long part = static_cast<long long>(it.qrow + rloc) * p.n_chunks + it.chunk;
+    __nv_bfloat16* orow = p.decode ? nullptr
+                                   : p.O + it.b * p.o_stride_b + it.h * p.o_stride_h +
+                                         static_cast<long long>(r) * p.o_stride_l + DH * g;
 #pragma unroll
     for (int cc = 0; cc < DH / 32; ++cc) {
       const uint32_t col = static_cast<uint32_t>(DH * g + cc * 32);
@@ -503,7 +550,19 @@ __device__ __forceinline__ void split_softmax_role(const int g, const AttnParams
 #pragma unroll
         for (int i = 0; i < 32; ++i) r1[i] = 0u;
       }
-      if (in_range) {
+      if (in_range && p.decode) {
+        float* prow = p.part_o + part * D + DH * g + cc * 32;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t y[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            y[e] = zero_row ? 0u
+                            : __float_as_uint(__uint_as_float(r0[4 * i + e]) * f0 +
+                                              __uint_as_float(r1[4 * i + e]) * f1);
+          st_global_v4(prow + 4 * i, y[0], y[1], y[2], y[3]);
+        }
+      } else if (in_range) {
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -518,7 +577,11 @@ __device__ __forceinline__ void split_softmax_role(const int g, const AttnParams
                        w[4 * i + 3]);
       }
     }
-    if (p.LSE != nullptr && in_range && g == 0) {
+    if (p.decode && in_range && g == 0) {
+      st_global_v4(p.part_ml + part * 4, __float_as_uint(zero_row ? -INFINITY : mm),
+                   __float_as_uint(zero_row ? 0.f : lsum), __float_as_uint(zero_row ? 0.f : lbsum),
+                   0u);
+    } else if (p.LSE != nullptr && in_range && g == 0) {
       const float lse = zero_row ? -INFINITY : (mm + log2f(lsum)) * 0.69314718055994530942f;
       p.LSE[(static_cast<long long>(it.b) * p.H + it.h) * p.Lq + r] = lse;
     }
@@ -609,6 +672,51 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, ATTN_TMEM_COLS);
   }
+}
+
+// ---------------------------------------------------------------------------
+// split-KV decode: merge the chunks' partial softmaxes of every query row
+// ---------------------------------------------------------------------------
+// One warp per query row (b, h, q); lane l holds output columns l, l + 32, ...
+// With m = max_c m_c and w_c = 2^(m_c - m):
+//   O = sum_c w_c Opart_c / sum_c w_c lb_c,   LSE = (m + log2 sum_c w_c l_c) ln 2,
+// the identity by which the online softmax merges partial results
+// ("Self-Attention 机制", Softmax 的数值稳定性与 Online Softmax).  Rows whose
+// every chunk is empty (padded or without keys) get O = 0 and LSE = -inf.
+template <int D>
+__global__ void __launch_bounds__(128)
+    attn_decode_combine_kernel(const float* __restrict__ part_o,
+                               const float* __restrict__ part_ml, int n_chunks, long long rows,
+                               __nv_bfloat16* __restrict__ O, float* __restrict__ LSE) {
+  constexpr int PER = D / 32;
+  const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  const int lane = static_cast<int>(threadIdx.x & 31u);
+  if (row >= rows) return;
+  const float* ml = part_ml + row * n_chunks * 4;
+  float mm = -INFINITY;
+  for (int c = 0; c < n_chunks; ++c) mm = fmaxf(mm, ml[c * 4]);
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  float l = 0.f, lb = 0.f;
+  if (mm != -INFINITY) {
+    for (int c = 0; c < n_chunks; ++c) {
+      const float mc = ml[c * 4];
+      if (mc == -INFINITY) continue;
+      const float w = ex2_approx(mc - mm);
+      l += w * ml[c * 4 + 1];
+      lb += w * ml[c * 4 + 2];
+      const float* po = part_o + (row * n_chunks + c) * D;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] += w * po[lane + 32 * i];
+    }
+  }
+  const bool zero = !(lb > 0.f);
+  const float inv = zero ? 0.f : 1.0f / lb;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) O[row * D + lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
+  if (LSE != nullptr && lane == 0)
+    LSE[row] = zero ? -INFINITY : (mm + log2f(l)) * 0.69314718055994530942f;
 }
 
 }  // namespace gb300

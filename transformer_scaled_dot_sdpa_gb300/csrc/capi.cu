@@ -334,6 +334,133 @@ attn_status_t attn_fwd_gqa(const void* Q, const void* K, const void* V, int B, i
                        osb, osh, osl, LSE, s);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Split-KV decode: chunk the keys so that there are about two work items per
+// SM over the B * h_kv (sequence, K/V head) pairs.
+struct DecodePlan {
+  int n_chunks;
+  int kv_chunk;  // keys per chunk, a multiple of 128
+};
+
+DecodePlan decode_plan(int num_sms, int B, int h_kv, int Lk) {
+  const long long pairs = static_cast<long long>(B) * h_kv;
+  const long long max_chunks = (static_cast<long long>(Lk) + 127) / 128;
+  long long n = (2ll * num_sms + pairs - 1) / pairs;
+  n = n < 1 ? 1 : (n > max_chunks ? max_chunks : n);
+  const int chunk = static_cast<int>(((Lk + n - 1) / n + 127) / 128 * 128);
+  return {static_cast<int>((Lk + chunk - 1) / chunk), chunk};
+}
+
+size_t decode_part_o_bytes(long long rows, int n_chunks, int d) {
+  return (static_cast<size_t>(rows) * n_chunks * d * 4 + 255) / 256 * 256;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_decode_workspace_bytes(int B, int h, int h_kv, int Lq, int Lk, int d) {
+  if (B <= 0 || h <= 0 || h_kv <= 0 || Lq <= 0 || Lk <= 0 || (d != 64 && d != 128)) return 0;
+  DeviceState* ds = nullptr;
+  if (device_state(&ds, nullptr) != ATTN_OK) return 0;
+  const DecodePlan plan = decode_plan(ds->num_sms, B, h_kv, Lk);
+  const long long rows = static_cast<long long>(B) * h * Lq;
+  return decode_part_o_bytes(rows, plan.n_chunks, d) +
+         static_cast<size_t>(rows) * plan.n_chunks * 4 * sizeof(float);
+}
+
+attn_status_t attn_decode(const void* Q, const void* K, const void* V, int B, int h, int h_kv,
+                          int Lq, int Lk, int d, int mask_kind, const int32_t* kv_lens,
+                          float scale, void* O, float* LSE, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  // ---- host-side validation (no CUDA call before this point) ----
+  if (B < 0 || h < 0 || Lq < 0 || Lk < 0) return ATTN_ERR_INVALID_ARG;
+  if (h_kv < 1 || (h > 0 && h % h_kv != 0)) return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_PADDING | ATTN_MASK_CAUSAL_BOTTOM_RIGHT)) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ATTN_MASK_CAUSAL) && (mask_kind & ATTN_MASK_CAUSAL_BOTTOM_RIGHT))
+    return ATTN_ERR_INVALID_ARG;
+  if (!(scale == scale) || std::isinf(scale)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (h > 0 && static_cast<long long>(h / h_kv) * Lq > gb300::SPLIT_ROWS)
+    return ATTN_ERR_UNSUPPORTED;  // the query rows of one K/V head fill one 128-row tile
+  if (static_cast<long long>(B) * h * Lq >= (1ll << 31) || static_cast<long long>(B) * h_kv *
+                                                               ((static_cast<long long>(Lk) + 127) / 128) >= (1ll << 31))
+    return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || h == 0 || Lq == 0) return ATTN_OK;
+  if (!O) return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ATTN_MASK_PADDING) && !kv_lens) return ATTN_ERR_INVALID_ARG;
+  if (Lk > 0 && (!Q || !K || !V || !workspace)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(O, 16) || (LSE && !aligned(LSE, 4)) || (kv_lens && !aligned(kv_lens, 4)))
+    return ATTN_ERR_MISALIGNED;
+  if (Lk > 0 && (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) ||
+                 !aligned(workspace, 256)))
+    return ATTN_ERR_MISALIGNED;
+
+  DeviceState* ds = nullptr;
+  attn_status_t st = device_state(&ds, nullptr);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (Lk == 0) {
+    const long long osl = d, osh = static_cast<long long>(Lq) * d, osb = osh * h;
+    gb300::attn_empty_keys_kernel<<<256, 256, 0, s>>>(static_cast<__nv_bfloat16*>(O), osb, osh,
+                                                     osl, LSE, B, h, Lq, d);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+  if (workspace_bytes < attn_decode_workspace_bytes(B, h, h_kv, Lq, Lk, d))
+    return ATTN_ERR_INVALID_ARG;
+  const DecodePlan plan = decode_plan(ds->num_sms, B, h_kv, Lk);
+  const long long rows = static_cast<long long>(B) * h * Lq;
+
+  CUtensorMap mq, mk, mv;
+  if ((st = map_2d(&mq, Q, static_cast<int>(rows), d, 64, 128)) != ATTN_OK) return st;
+  if ((st = map_bhld(&mk, K, B, h_kv, Lk, d)) != ATTN_OK) return st;
+  if ((st = map_bhld(&mv, V, B, h_kv, Lk, d)) != ATTN_OK) return st;
+
+  gb300::AttnParams p;
+  std::memset(&p, 0, sizeof p);
+  p.B = B;
+  p.H = h;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.kv_group = h / h_kv;
+  p.causal_offset = (mask_kind & ATTN_MASK_CAUSAL_BOTTOM_RIGHT) ? (Lk - Lq) : 0;
+  p.mask_kind = (mask_kind & ATTN_MASK_PADDING) |
+                ((mask_kind & (ATTN_MASK_CAUSAL | ATTN_MASK_CAUSAL_BOTTOM_RIGHT)) ? 1 : 0);
+  p.kv_lens = kv_lens;
+  const double sc = scale > 0.f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(d));
+  p.scale_log2 = static_cast<float>(sc * 1.4426950408889634074);
+  p.status = ds->status;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    p.wait_limit_ns = g_wait_limit_ns;
+    p.debug_skip_kv_load = g_debug_skip_kv_load;
+  }
+  p.decode = 1;
+  p.q_rows = p.kv_group * Lq;
+  p.kv_chunk = plan.kv_chunk;
+  p.n_chunks = plan.n_chunks;
+  p.n_qblocks = 1;
+  p.n_items = static_cast<int>(static_cast<long long>(B) * h_kv * plan.n_chunks);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.part_o = reinterpret_cast<float*>(ws);
+  p.part_ml = reinterpret_cast<float*>(ws + decode_part_o_bytes(rows, plan.n_chunks, d));
+  st = d == 64 ? launch_attn<64, ATTN_SCHEDULE_SPLIT_KEYS>(ds, mq, mk, mv, p, s)
+               : launch_attn<128, ATTN_SCHEDULE_SPLIT_KEYS>(ds, mq, mk, mv, p, s);
+  if (st != ATTN_OK) return st;
+  const unsigned grid = static_cast<unsigned>((rows + 3) / 4);
+  if (d == 64)
+    gb300::attn_decode_combine_kernel<64><<<grid, 128, 0, s>>>(
+        p.part_o, p.part_ml, plan.n_chunks, rows, static_cast<__nv_bfloat16*>(O), LSE);
+  else
+    gb300::attn_decode_combine_kernel<128><<<grid, 128, 0, s>>>(
+        p.part_o, p.part_ml, plan.n_chunks, rows, static_cast<__nv_bfloat16*>(O), LSE);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 attn_status_t attn_weights(const void* Q, const void* K, const float* LSE, int B, int h,
                            int h_kv, int Lq, int Lk, int d_k, int mask_kind,
                            const int32_t* kv_lens, float scale, float* A, void* stream) {
