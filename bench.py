@@ -32,8 +32,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from sdpa_workloads import (BENCH_WORKLOAD, MASK_CAUSAL, MASK_PADDING, WORKLOADS,  # noqa: E402
-                            attn_flops, make_workload_inputs)
+from sdpa_workloads import (BENCH_WORKLOAD, MASK_CAUSAL, MASK_CAUSAL_BOTTOM_RIGHT,  # noqa: E402
+                            MASK_PADDING, WORKLOADS, attn_flops, make_workload_inputs)
 
 METRIC = "attention fwd TFLOP/s on 1 GB300 and % of roofline (tensor/exp/HBM bound)"
 UNIT = "TFLOP/s"
@@ -81,8 +81,29 @@ def attention_kernel_name(B, H, Lq, d):
     return ("attn_fwd_split_kernel<%d>" if split else "attn_fwd_kernel<%d>") % d
 
 
+def visible_keys(w, i, kv_len):
+    """Keys query row i of a sequence with kv_len valid keys attends to (0 for
+    a padded row), under the workload's mask."""
+    n = w.Lk
+    if w.mask_kind & MASK_CAUSAL:
+        n = min(n, i + 1)
+    if w.mask_kind & MASK_CAUSAL_BOTTOM_RIGHT:
+        n = min(n, max(i + 1 + w.Lk - w.Lq, 0))
+    if w.mask_kind & MASK_PADDING:
+        n = 0 if i >= kv_len else min(n, kv_len)
+    return n
+
+
 def algorithmic_counts(w, kv_lens):
     """FLOPs, exponentials and HBM bytes of one pass (definitions in the design doc)."""
+    if w.kind == "decode":
+        # 4*d FLOPs and one exp per visible (row, key) pair; the cache's valid
+        # K/V rows read once per K/V head, Q read and O, LSE written once
+        lens = [int(n) for n in kv_lens] if kv_lens is not None else [w.Lk] * w.B
+        pairs = sum(w.H * visible_keys(w, i, n) for n in lens for i in range(w.Lq))
+        kv_bytes = sum(2.0 * w.H_kv * n * w.d_k * 2 for n in lens)
+        io_bytes = 2.0 * w.B * w.H * w.Lq * w.d_k * 2 + 4.0 * w.B * w.H * w.Lq
+        return 4.0 * w.d_k * pairs, float(pairs), kv_bytes + io_bytes
     flops = attn_flops(w.B, w.H, w.Lq, w.Lk, w.d_k, w.mask_kind, kv_lens)
     exps = flops / (4.0 * w.d_k)            # one exp per unmasked score
     qkv_bytes = 2.0 * w.B * w.H * (w.Lq * w.d_k + w.Lk * (w.d_k + w.d_v))
@@ -228,12 +249,7 @@ def oracle_row_flops(w, rows, kv_lens):
     for r in rows:
         i = int(r % w.Lq)
         b = int(r // (w.H * w.Lq))
-        n = w.Lk
-        if w.mask_kind & MASK_CAUSAL:
-            n = min(n, i + 1)
-        if w.mask_kind & MASK_PADDING:
-            n = 0 if i >= kv_lens[b] else min(n, int(kv_lens[b]))
-        tot += 4.0 * n * w.d_k
+        tot += 4.0 * visible_keys(w, i, int(kv_lens[b]) if kv_lens is not None else w.Lk) * w.d_k
     return tot
 
 
@@ -279,17 +295,23 @@ def reference_arm(args, w):
 
 
 def attn_input_bytes(w):
-    return 2 * w.B * w.H * (w.Lq + 2 * w.Lk) * w.d_k
+    h_kv = getattr(w, "H_kv", w.H)
+    return 2 * w.B * (w.H * w.Lq + 2 * h_kv * w.Lk) * w.d_k
 
 
 def workload_config(w, world, flushed=False):
-    mask = {0: "none", 1: "causal", 2: "padding", 3: "causal+padding"}[w.mask_kind]
+    mask = {0: "none", 1: "causal", 2: "padding", 3: "causal+padding",
+            4: "causal (bottom-right)", 6: "causal (bottom-right)+padding"}[w.mask_kind]
     mb = attn_input_bytes(w) / 1e6
     l2 = ("Q/K/V %.1f MB fit in L2: L2 flushed (a 2x L2 buffer rewritten) before every timed "
           "call, outside its events" % mb if flushed else
           "inputs larger than L2 (Q/K/V %.0f MB), no flush" % mb)
-    return {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d_k,
-            "mask": mask, "parallelism": "replicas x%d" % world, "l2": l2}
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d_k,
+           "mask": mask, "parallelism": "replicas x%d" % world, "l2": l2}
+    if w.kind == "decode":
+        cfg["H_kv"] = w.H_kv
+        cfg["call"] = "attn_decode (split over the keys)"
+    return cfg
 
 
 # ---------------------------------------------------------------------------
@@ -321,10 +343,18 @@ def ours_arm(args, w):
     O = torch.empty((w.B, w.H, w.Lq, w.d_v), dtype=torch.bfloat16, device=dev)
     LSE = torch.empty((w.B, w.H, w.Lq), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    decode = w.kind == "decode"
+    if decode:
+        ws = torch.empty(g.attn_decode_workspace_bytes(w.B, w.H, w.H_kv, w.Lq, w.Lk, w.d_k),
+                         dtype=torch.uint8, device=dev)
 
     def step():
-        g.attn_fwd(q, k, v, mask_kind=w.mask_kind, kv_lens=kvt, scale=w.scale, out=O, lse=LSE,
-                   stream=stream)
+        if decode:
+            g.attn_decode(q, k, v, mask_kind=w.mask_kind, kv_lens=kvt, scale=w.scale, out=O,
+                          lse=LSE, workspace=ws, stream=stream)
+        else:
+            g.attn_fwd(q, k, v, mask_kind=w.mask_kind, kv_lens=kvt, scale=w.scale, out=O,
+                       lse=LSE, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -391,7 +421,8 @@ def ours_arm(args, w):
         "unit": "TFLOP/s" if bound != "hbm" else "GB/s",
         "traffic": profiled_traffic(w.name),
         "peak_source": "%s (bf16 dense burst)" % peak_src if bound != "hbm" else peak_src,
-        "kernel": attention_kernel_name(w.B, w.H, w.Lq, w.d_k),
+        "kernel": ("attn_fwd_split_kernel<%d> (decode mode)" % w.d_k if w.kind == "decode"
+                   else attention_kernel_name(w.B, w.H, w.Lq, w.d_k)),
         "roofline_time_ms": 1e3 * max(t_tensor, t_exp, t_hbm),
         "frac_of_roofline_time": 1e3 * max(t_tensor, t_exp, t_hbm) / ms,
         "exp_bound_fraction": t_exp / max(t_tensor, t_hbm),
@@ -414,7 +445,7 @@ def ours_arm(args, w):
                 "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
                 "d2h_bytes_per_step": int(hO.numel() * 2 + hL.numel() * 4),
                 "steps": e2e_steps, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps,
+        "gpu_launches": (2 if w.kind == "decode" else 1) * args.steps,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "clocks": clk,

@@ -25,6 +25,7 @@ import numpy as np
 MASK_NONE = 0
 MASK_CAUSAL = 1
 MASK_PADDING = 2
+MASK_CAUSAL_BOTTOM_RIGHT = 4
 
 
 # ---------------------------------------------------------------------------
@@ -79,6 +80,32 @@ class AttnWorkload:
 
 
 @dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """One decoding step: Lq new query rows per sequence against a K/V cache
+    of Lk rows (valid lengths drawn from kv_len_range), H query heads on H_kv
+    K/V heads, causal aligned to each cache's last key."""
+    name: str
+    B: int
+    H: int
+    H_kv: int
+    Lq: int
+    Lk: int
+    d_k: int
+    mask_kind: int
+    seed: int
+    kv_len_range: Optional[tuple] = None
+    scale: Optional[float] = None
+
+    @property
+    def kind(self) -> str:
+        return "decode"
+
+    @property
+    def d_v(self) -> int:
+        return self.d_k
+
+
+@dataclasses.dataclass(frozen=True)
 class LayerWorkload:
     """Full multi-head layer: X.W_QKV -> split heads -> SDPA -> concat -> .W_O."""
     name: str
@@ -113,6 +140,9 @@ WORKLOADS = {
                      boost_frac=0.05, boost=3.0),
         LayerWorkload("mha_layer_causal_b8_l2048_dm1024_h16", B=8, L=2048, d_model=1024, H=16,
                       mask_kind=MASK_CAUSAL, seed=1005, w_std=1.0 / 32.0),
+        DecodeWorkload("gqa_decode_b8_h32_hkv8_lq1_lk32768_d128", B=8, H=32, H_kv=8, Lq=1,
+                       Lk=32768, d_k=128, mask_kind=MASK_CAUSAL_BOTTOM_RIGHT | MASK_PADDING,
+                       seed=1006, kv_len_range=(16384, 32768)),
     ]
 }
 
@@ -177,6 +207,9 @@ def make_workload_inputs(w):
         return make_attention_inputs(w.B, w.H, w.Lq, w.Lk, w.d_k, w.d_v, w.seed,
                                      kv_len_range=w.kv_len_range,
                                      boost_frac=w.boost_frac, boost=w.boost)
+    if w.kind == "decode":
+        return make_attention_inputs(w.B, w.H, w.Lq, w.Lk, w.d_k, w.d_k, w.seed,
+                                     kv_len_range=w.kv_len_range, H_kv=w.H_kv)
     return make_layer_inputs(w.B, w.L, w.d_model, w.seed, w.w_std)
 
 

@@ -338,8 +338,12 @@ attn_status_t attn_fwd_gqa(const void* Q, const void* K, const void* V, int B, i
 
 namespace {
 
-// Split-KV decode: chunk the keys so that there are about two work items per
-// SM over the B * h_kv (sequence, K/V head) pairs.
+// Split-KV decode: chunk the keys into about `per_sm` work items per SM over
+// the B * h_kv (sequence, K/V head) pairs.  per_sm follows a sweep on GB300
+// (GQA, d = 128): one item per SM was best with 8-16 pairs (4.7 TB/s at 8
+// pairs, 3.0 with six); with 32-64 pairs three to five were best and four
+// was within 6% of the best everywhere (5.4 TB/s, 3.9-4.9 with one), also
+// with cache lengths that vary between sequences.
 struct DecodePlan {
   int n_chunks;
   int kv_chunk;  // keys per chunk, a multiple of 128
@@ -348,7 +352,8 @@ struct DecodePlan {
 DecodePlan decode_plan(int num_sms, int B, int h_kv, int Lk) {
   const long long pairs = static_cast<long long>(B) * h_kv;
   const long long max_chunks = (static_cast<long long>(Lk) + 127) / 128;
-  long long n = (2ll * num_sms + pairs - 1) / pairs;
+  const long long per_sm = pairs < 24 ? 1 : 4;
+  long long n = (per_sm * num_sms + pairs - 1) / pairs;
   n = n < 1 ? 1 : (n > max_chunks ? max_chunks : n);
   const int chunk = static_cast<int>(((Lk + n - 1) / n + 127) / 128 * 128);
   return {static_cast<int>((Lk + chunk - 1) / chunk), chunk};
