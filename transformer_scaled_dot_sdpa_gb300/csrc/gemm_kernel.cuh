@@ -9,9 +9,9 @@
 //
 // CTA organisation (persistent, one CTA per SM):
 //   warp 0      TMA producer (one thread): A and B tiles into a 4-stage ring
-//   warp 1      MMA issuer (one thread) + TMEM owner; two 256-column fp32
-//               accumulators so the epilogue of one tile overlaps the
-//               main loop of the next
+//   warp 1      MMA issuer (whole warp, one elected lane issues) + TMEM
+//               owner; two 256-column fp32 accumulators so the epilogue of
+//               one tile overlaps the main loop of the next
 //   warps 2-5   epilogue: TMEM -> registers -> bf16 -> global, one row each
 #pragma once
 
@@ -131,43 +131,47 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, GEMM_BN, true);
-      const uint32_t a_base = smem_u32(smem + L::A_OFF);
-      const uint32_t b_base = smem_u32(smem + L::B_OFF);
-      uint32_t it = 0, tcount = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x, ++tcount) {
-        const uint32_t acc = tcount & 1u;
-        if (tcount >= 2u) {
-          ok = mbar_wait(&bars[L::B_ACC_EMPTY + acc], ((tcount >> 1) - 1u) & 1u, ctl);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        const uint32_t d_tmem = tmem + acc * GEMM_BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
-          const int s = static_cast<int>(it % GEMM_STAGES);
-          ok = mbar_wait(&bars[L::B_FULL + s], (it / GEMM_STAGES) & 1u, ctl);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t aa = a_base + s * L::A_BYTES;
-          const uint32_t ba = b_base + s * L::B_BYTES;
+    // ---------------- MMA issuer ----------------
+    // The whole warp waits and computes operands; one elected lane issues,
+    // so the operands stay warp-uniform and each MMA issues quickly.
+    constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, GEMM_BN, true);
+    constexpr unsigned FULL = 0xffffffffu;
+    const uint64_t a_desc = smem_desc_sw128(smem_u32(smem + L::A_OFF), 16, 1024);
+    const uint64_t b_desc = smem_desc_sw128(smem_u32(smem + L::B_OFF), L::B_CHUNK, 1024);
+    uint32_t it = 0, tcount = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x, ++tcount) {
+      const uint32_t acc = tcount & 1u;
+      if (tcount >= 2u) {
+        ok = __all_sync(FULL, mbar_wait(&bars[L::B_ACC_EMPTY + acc], ((tcount >> 1) - 1u) & 1u, ctl));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      const uint32_t d_tmem = tmem + acc * GEMM_BN;
+      for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+        const int s = static_cast<int>(it % GEMM_STAGES);
+        ok = __all_sync(FULL, mbar_wait(&bars[L::B_FULL + s], (it / GEMM_STAGES) & 1u, ctl));
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t ad = a_desc + static_cast<uint64_t>((s * L::A_BYTES) >> 4);
+        const uint64_t bd = b_desc + static_cast<uint64_t>((s * L::B_BYTES) >> 4);
+        if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < GEMM_BK / 16; ++kk) {
-            mma_bf16_ss(d_tmem, smem_desc_sw128(aa + kk * 32, 16, 1024),
-                        smem_desc_sw128(ba + kk * 2048, L::B_CHUNK, 1024), IDESC,
+          for (int kk = 0; kk < GEMM_BK / 16; ++kk)
+            mma_bf16_ss(d_tmem, ad + static_cast<uint64_t>((kk * 32) >> 4),
+                        bd + static_cast<uint64_t>((kk * 2048) >> 4), IDESC,
                         (kb > 0 || kk > 0) ? 1u : 0u);
-          }
           mma_commit(&bars[L::B_EMPTY + s]);
         }
-        if (!ok) break;
-        mma_commit(&bars[L::B_ACC_FULL + acc]);
+        __syncwarp();
       }
-      mma_commit(&bars[L::B_DRAIN]);
-      mbar_wait_drain(&bars[L::B_DRAIN], 0u, ctl.limit_ns);
+      if (!ok) break;
+      if (elect_one()) mma_commit(&bars[L::B_ACC_FULL + acc]);
+      __syncwarp();
     }
+    if (elect_one()) mma_commit(&bars[L::B_DRAIN]);
     __syncwarp();
+    mbar_wait_drain(&bars[L::B_DRAIN], 0u, ctl.limit_ns);
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int row = static_cast<int>((warp & 3) * 32 + lane);  // TMEM lane = tile row
