@@ -38,8 +38,11 @@ from sdpa_workloads import (BENCH_WORKLOAD, MASK_CAUSAL, MASK_CAUSAL_BOTTOM_RIGH
 METRIC = "attention fwd TFLOP/s on 1 GB300 and % of roofline (tensor/exp/HBM bound)"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-MUFU_EXP_PER_S = 10.7e12  # nominal ex2 rate of the part (not measured)
-KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "ptx.cuh"]
+# sources whose hash a committed DRAM-traffic figure is tied to, per kernel
+KERNEL_SOURCES = {
+    "attn_fwd_kernel": ["attn_fwd_kernel.cuh", "ptx.cuh"],
+    "attn_fwd_split_kernel": ["attn_fwd_split_kernel.cuh", "attn_fwd_kernel.cuh", "ptx.cuh"],
+}
 
 
 def load_peaks():
@@ -50,24 +53,29 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+def kernel_base_name(kernel):
+    return kernel.split("<")[0].strip()
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel_base_name(kernel)]:
         with open(os.path.join(ROOT, "transformer_scaled_dot_sdpa_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+def profiled_traffic(workload, kernel):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, if it was taken on that kernel's current source; else None."""
     path = os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     ent = d.get(workload)
-    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+    if (not ent or kernel_base_name(ent.get("kernel", "")) != kernel_base_name(kernel)
+            or ent.get("kernel_source_hash") != kernel_source_hash(kernel)):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -92,6 +100,41 @@ def visible_keys(w, i, kv_len):
     if w.mask_kind & MASK_PADDING:
         n = 0 if i >= kv_len else min(n, kv_len)
     return n
+
+
+def measure_ex2_rate(g, dev, stream):
+    """exp2 per second of the whole GPU from the library's ex2 probe (as many
+    512-thread CTAs as the SMs hold at once, 8 independent chains per thread;
+    median of 5 timed launches), with the SM clock the probe ran at (cycles /
+    nanoseconds inside each CTA) and the rate per clock per SM."""
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    threads = 512
+    per_sm = max(1, getattr(props, "max_threads_per_multi_processor", 1536) // threads)
+    blocks, iters = per_sm * sms, 4096 // per_sm
+    timing = torch.zeros(2 * blocks, dtype=torch.int64, device=dev)
+    sink = torch.zeros(1, dtype=torch.float32, device=dev)
+    n_exp = float(blocks) * threads * iters * g.PROBE_EX2_PER_THREAD_ITER
+    for _ in range(2):
+        g.probe_ex2(blocks, threads, iters, timing, sink, stream)
+    times = []
+    for _ in range(5):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.probe_ex2(blocks, threads, iters, timing, sink, stream)
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e-3)
+    g.check_device_status(stream)
+    sec = sorted(times)[len(times) // 2]
+    t = timing.view(blocks, 2).double()
+    clock_hz = float((t[:, 0] / t[:, 1]).median().item()) * 1e9
+    rate = n_exp / sec
+    return {"exp_per_s": rate, "sm_mhz": clock_hz / 1e6,
+            "exp_per_clk_per_sm": rate / (sms * clock_hz), "exps_per_launch": n_exp,
+            "ms_per_launch": sec * 1e3}
 
 
 def algorithmic_counts(w, kv_lens):
@@ -356,6 +399,7 @@ def ours_arm(args, w):
             g.attn_fwd(q, k, v, mask_kind=w.mask_kind, kv_lens=kvt, scale=w.scale, out=O,
                        lse=LSE, stream=stream)
 
+    ex2 = measure_ex2_rate(g, dev, stream)  # denominator of the roofline's exp term
     for _ in range(args.warmup):
         step()
     g.check_device_status(stream)
@@ -410,22 +454,25 @@ def ours_arm(args, w):
     tensor_peak = peaks["bf16_tflops"] * 1e12
     hbm_peak = peaks["hbm_gbs"] * 1e9
     t_tensor = flops / tensor_peak
-    t_exp = exps / MUFU_EXP_PER_S
+    t_exp = exps / ex2["exp_per_s"]
     t_hbm = hbm_bytes / hbm_peak
     bound = max((t_tensor, "tensor"), (t_hbm, "hbm"), (t_exp, "exp"))[1]
     achieved_tflops = flops / (ms * 1e-3) / 1e12   # this rank's kernel
+    kernel = ("attn_fwd_split_kernel<%d> (decode mode)" % w.d_k if w.kind == "decode"
+              else attention_kernel_name(w.B, w.H, w.Lq, w.d_k))
     roofline = {
         "bound": "tensor" if bound in ("tensor", "exp") else "hbm",
         "achieved": achieved_tflops if bound != "hbm" else hbm_bytes / (ms * 1e-3) / 1e9,
         "peak": peaks["bf16_tflops"] if bound != "hbm" else peaks["hbm_gbs"],
         "unit": "TFLOP/s" if bound != "hbm" else "GB/s",
-        "traffic": profiled_traffic(w.name),
         "peak_source": "%s (bf16 dense burst)" % peak_src if bound != "hbm" else peak_src,
-        "kernel": ("attn_fwd_split_kernel<%d> (decode mode)" % w.d_k if w.kind == "decode"
-                   else attention_kernel_name(w.B, w.H, w.Lq, w.d_k)),
+        "kernel": kernel,
+        "traffic": profiled_traffic(w.name, kernel),
         "roofline_time_ms": 1e3 * max(t_tensor, t_exp, t_hbm),
         "frac_of_roofline_time": 1e3 * max(t_tensor, t_exp, t_hbm) / ms,
         "exp_bound_fraction": t_exp / max(t_tensor, t_hbm),
+        "exp_rate": {"exp_per_s": ex2["exp_per_s"], "exp_per_clk_per_sm": ex2["exp_per_clk_per_sm"],
+                     "sm_mhz": ex2["sm_mhz"], "source": "measured (attn_probe_ex2)"},
     }
     roofline["frac"] = roofline["achieved"] / roofline["peak"]
 

@@ -293,6 +293,31 @@ attn_status_t attn_set_schedule(int schedule);
  */
 void attn_debug_skip_kv_load(long long index);
 
+/*
+ * attn_probe_ex2 -- diagnostic: measures the throughput of the special-
+ * function unit's exp2 (ex2.approx.ftz.f32), the one transcendental the
+ * softmax issues per unmasked score, so that the exp term of the attention
+ * roofline (exp count / exp rate) uses a measured rate.
+ *
+ * Launches `blocks` CTAs of `threads` threads on `stream`; every thread runs
+ * `iters` iterations of ATTN_PROBE_EX2_PER_THREAD_ITER (= 32) ex2 in 8
+ * independent chains, so one launch performs
+ * blocks * threads * iters * 32 exp2.  The caller times the launch with
+ * events on `stream`.
+ *   timing_out  device, uint64 [blocks][2]: for each CTA, the SM clock
+ *               cycles (clock64) and the nanoseconds (globaltimer) it spent
+ *               in its loop, both between the same two CTA barriers; their
+ *               ratio is the SM clock during the probe
+ *   sink        device, one float: never written in practice (it keeps the
+ *               chains' results live)
+ * Errors: ATTN_ERR_INVALID_ARG for blocks < 1, iters < 1, threads not a
+ * multiple of 32 in [32, 1024], or a NULL pointer; ATTN_ERR_CUDA if the launch
+ * fails.  Asynchronous, like the other entry points.
+ */
+#define ATTN_PROBE_EX2_PER_THREAD_ITER 32
+attn_status_t attn_probe_ex2(int blocks, int threads, int iters,
+                             unsigned long long* timing_out, float* sink, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -144,3 +144,20 @@ def test_decode_validation(cdll):
     bad = ctypes.c_void_p(0x1080)  # 16-byte but not 256-byte aligned workspace
     assert f(p, p, p, 1, 8, 2, 1, 64, 128, 4, None, 0.0, p, None, bad, 1 << 20, None) == MISALIGNED
     assert f(None, None, None, 0, 8, 2, 1, 64, 128, 4, None, 0.0, None, None, None, 0, None) == 0
+
+
+def test_probe_ex2_validation(cdll):
+    f = cdll.attn_probe_ex2
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p]
+    dummy = ctypes.c_void_p(256)  # never dereferenced: every case fails validation first
+    for blocks, threads, iters, cyc, sink in [
+            (0, 1024, 1, dummy, dummy),     # no CTA
+            (1, 1024, 0, dummy, dummy),     # no iteration
+            (1, 48, 1, dummy, dummy),       # not whole warps
+            (1, 2048, 1, dummy, dummy),     # above the CTA limit
+            (1, 0, 1, dummy, dummy),
+            (1, 1024, 1, None, dummy),      # NULL cycles
+            (1, 1024, 1, dummy, None)]:     # NULL sink
+        assert f(blocks, threads, iters, cyc, sink, None) == 1

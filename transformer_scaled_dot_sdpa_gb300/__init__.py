@@ -23,7 +23,7 @@ __all__ = [
     "attn_weights", "mha_layer_fwd",
     "mha_layer_workspace_bytes", "mha_layer_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gemm_bf16",
     "check_device_status", "set_wait_limit_ns", "set_schedule", "SCHEDULE_AUTO",
-    "SCHEDULE_TWO_QTILES", "SCHEDULE_SPLIT_KEYS", "debug_skip_kv_load", "library_path", "lib",
+    "SCHEDULE_TWO_QTILES", "SCHEDULE_SPLIT_KEYS", "debug_skip_kv_load", "probe_ex2", "PROBE_EX2_PER_THREAD_ITER", "library_path", "lib",
 ]
 
 MASK_NONE = 0
@@ -91,6 +91,8 @@ def _load():
     L.attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.attn_set_schedule.restype = i32
     L.attn_set_schedule.argtypes = [i32]
+    L.attn_probe_ex2.restype = i32
+    L.attn_probe_ex2.argtypes = [i32, i32, i32, vp, vp, vp]
     L.attn_debug_skip_kv_load.restype = None
     L.attn_debug_skip_kv_load.argtypes = [i64]
     return L
@@ -305,3 +307,20 @@ def set_schedule(schedule):
 
 def debug_skip_kv_load(index):
     lib.attn_debug_skip_kv_load(int(index))
+
+
+PROBE_EX2_PER_THREAD_ITER = 32  # exp2 per thread per iteration of the probe
+
+
+def probe_ex2(blocks, threads, iters, timing, sink, stream=None):
+    """Launch the exp2 throughput probe: ``blocks`` CTAs of ``threads`` threads,
+    ``blocks * threads * iters * PROBE_EX2_PER_THREAD_ITER`` exp2 in all.
+    ``timing`` is a contiguous 8-byte-element CUDA tensor of ``2 * blocks``
+    elements (SM cycles and nanoseconds of each CTA), ``sink`` a float32 CUDA
+    tensor of at least one element."""
+    if (timing.numel() < 2 * blocks or timing.element_size() != 8 or not timing.is_cuda
+            or not timing.is_contiguous()):
+        raise ValueError("timing must be a contiguous CUDA tensor of >= 2*blocks 8-byte elements")
+    _dev_tensor(sink, "sink", torch.float32)
+    _check(lib.attn_probe_ex2(int(blocks), int(threads), int(iters), _ptr(timing), _ptr(sink),
+                              _stream_handle(stream)), "attn_probe_ex2")

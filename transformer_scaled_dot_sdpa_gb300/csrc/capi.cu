@@ -14,6 +14,7 @@
 #include "attn_fwd_split_kernel.cuh"
 #include "attn_weights_kernel.cuh"
 #include "gemm_kernel.cuh"
+#include "probe_kernel.cuh"
 
 namespace {
 
@@ -276,6 +277,18 @@ attn_status_t attn_set_schedule(int schedule) {
   std::lock_guard<std::mutex> lock(g_mutex);
   g_schedule = schedule;
   return ATTN_OK;
+}
+
+attn_status_t attn_probe_ex2(int blocks, int threads, int iters,
+                             unsigned long long* timing_out, float* sink, void* stream) {
+  static_assert(gb300::PROBE_CHAINS * gb300::PROBE_EX2_PER_LINK == ATTN_PROBE_EX2_PER_THREAD_ITER,
+                "exp2 per thread and iteration");
+  if (blocks < 1 || iters < 1 || threads < 32 || threads > 1024 || threads % 32 != 0 ||
+      timing_out == nullptr || sink == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  gb300::ex2_probe_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      iters, timing_out, sink);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 void attn_debug_skip_kv_load(long long index) {
