@@ -22,11 +22,15 @@
 //   warp 11        = idle (it completes the third warpgroup, which the
 //                    per-warpgroup register reallocation needs)
 // TMEM (512 columns x 128 lanes, fp32):
-//   [  0,128) S of tile 0; P (bf16 pairs) reuses its high 64 columns
-//   [128,256) S / P of tile 1
-//   [256,384) O accumulator of tile 0, [384,512) O of tile 1
+//   [  0,128) S of tile 0, [128,256) S of tile 1
+//   D = 128: P (bf16 pairs) reuses the high 64 columns of its S;
+//            [256,384) O accumulator of tile 0, [384,512) O of tile 1
+//   D = 64:  [256,320) O of tile 0, [320,384) O of tile 1, and P has columns
+//            of its own: [384,448) P of tile 0, [448,512) P of tile 1
 // Each Q tile has its own MMA issuer; while one softmax group works on its
-// S, the tensor core runs the other tile's P.V and next S.
+// S, the tensor core runs the other tile's P.V and next S.  At D = 64 the
+// separate P columns also let S_t(j+1) start as soon as the softmax has read
+// S_t(j) ("early S"), so it overlaps that softmax's exponentials.
 //
 // Softmax state per row (one thread per row = one TMEM lane): m in log2
 // units (already multiplied by scale*log2 e) and two running sums: l of the
@@ -110,7 +114,19 @@ struct AttnLayout {
   static constexpr int B_P_FULL = B_S_FULL + 2;
   static constexpr int B_O_DONE = B_P_FULL + 2;
   static constexpr int B_DRAIN = B_O_DONE + 2;  // one per MMA issuer
-  static constexpr int N_BARS = B_DRAIN + 2;
+  static constexpr int B_S_EMPTY = B_DRAIN + 2;  // [tile], early-S schedule only
+  static constexpr int B_PV_DONE = B_S_EMPTY + 2;  // [tile], early-S schedule only
+  static constexpr int N_BARS = B_PV_DONE + 2;
+  // Early-S schedule (D = 64): P has TMEM columns of its own, so S_t(j+1) is
+  // issued as soon as the softmax has read S_t(j) into registers and runs on
+  // the tensor core while that softmax computes its exponentials.
+  static constexpr bool EARLY_S = (D == 64);
+  // TMEM columns of tile t: S at 128 t; O at 256 + O_STRIDE t; P (bf16
+  // pairs) at p_col(t): the high half of S_t, or its own 64 columns
+  static constexpr uint32_t O_STRIDE = EARLY_S ? 64u : 128u;
+  static __device__ __forceinline__ uint32_t p_col(int t) {
+    return EARLY_S ? 384u + 64u * static_cast<uint32_t>(t) : 128u * static_cast<uint32_t>(t) + 64u;
+  }
   static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
 };
@@ -292,10 +308,11 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
   const uint64_t k_desc = smem_desc_sw128(smem_u32(smem + L::K_OFF), 16, 1024);
   const uint64_t v_desc = smem_desc_sw128(smem_u32(smem + L::V_OFF), L::CHUNK_BYTES, 1024);
   const uint32_t s_tmem = tmem + static_cast<uint32_t>(t * ATTN_BLOCK_N);
-  const uint32_t p_tmem = s_tmem + 64u;  // P in the high half of the S columns
-  const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(t * 128);
+  const uint32_t p_tmem = tmem + L::p_col(t);
+  const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(t) * L::O_STRIDE;
   constexpr unsigned FULL = 0xffffffffu;
   uint32_t q_uses = 0, p_cnt = 0;
+  uint32_t s_issued = 0;  // S MMAs issued (early-S: S_EMPTY phases to wait for)
   uint32_t kv_it = 0;  // running KV tile index (stage = kv_it % STAGES)
   bool ok = true;
   AttnItem it;
@@ -325,6 +342,8 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
       if (ok && nkv > 0) {
         ok = __all_sync(FULL, mbar_wait(&bars[L::B_Q_FULL + t], q_uses & 1u, ctl));
         ++q_uses;
+        if (L::EARLY_S && ok && s_issued > 0)
+          ok = __all_sync(FULL, mbar_wait(&bars[L::B_S_EMPTY + t], (s_issued - 1u) & 1u, ctl));
         if (ok) {
           tc_fence_after();
           if (elect_one()) {
@@ -333,11 +352,30 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
             if (nkv == 1) mma_commit(&bars[L::B_Q_EMPTY + t]);
           }
           __syncwarp();
+          ++s_issued;
         }
       }
     }
     for (int j = 0; ok && j < it.nkv_max; ++j, ++kv_it) {
       const int s = static_cast<int>(kv_it % L::STAGES);
+      if (L::EARLY_S && j + 1 < nkv) {
+        // S_t(j+1) as soon as the softmax has read S_t(j) into registers: it
+        // runs on the tensor core while that softmax computes P_t(j)
+        const uint32_t kv = kv_it + 1u;
+        const int s1 = static_cast<int>(kv % L::STAGES);
+        ok = __all_sync(FULL, mbar_wait(&bars[L::B_S_EMPTY + t], (s_issued - 1u) & 1u, ctl));
+        if (!ok) break;
+        ok = __all_sync(FULL, mbar_wait(&bars[L::B_K_FULL + s1], (kv / L::STAGES) & 1u, ctl));
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one()) {
+          issue_s(s1);
+          mma_commit(&bars[L::B_S_FULL + t]);
+          if (j + 2 == nkv) mma_commit(&bars[L::B_Q_EMPTY + t]);
+        }
+        __syncwarp();
+        ++s_issued;
+      }
       ok = __all_sync(FULL, mbar_wait(&bars[L::B_V_FULL + s], (kv_it / L::STAGES) & 1u, ctl));
       if (!ok) break;
       if (j < nkv) {
@@ -355,6 +393,7 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
           // K_j (read by S_t(j), issued earlier) and V_j are free once this
           // P.V completes; O_t is final after the item's last P.V
           mma_commit(&bars[L::B_KV_EMPTY + s]);
+          if (L::EARLY_S) mma_commit(&bars[L::B_PV_DONE + t]);
           if (j == nkv - 1) mma_commit(&bars[L::B_O_DONE + t]);
         }
         __syncwarp();
@@ -362,7 +401,7 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
         if (elect_one()) mbar_arrive(&bars[L::B_KV_EMPTY + s]);
         __syncwarp();
       }
-      if (j + 1 < it.nkv_max) {
+      if (!L::EARLY_S && j + 1 < it.nkv_max) {
         const int s1 = static_cast<int>((kv_it + 1) % L::STAGES);
         ok = __all_sync(FULL,
                         mbar_wait(&bars[L::B_K_FULL + s1], ((kv_it + 1) / L::STAGES) & 1u, ctl));
@@ -396,8 +435,8 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
   const int rloc = static_cast<int>(threadIdx.x & 127u);
   const uint32_t lane_base = static_cast<uint32_t>(threadIdx.x & 96u) << 16;
   const uint32_t s_tmem = tmem + static_cast<uint32_t>(t * ATTN_BLOCK_N) + lane_base;
-  const uint32_t p_tmem = s_tmem + 64u;  // P in the high half of the S columns
-  const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(t * 128) + lane_base;
+  const uint32_t p_tmem = tmem + L::p_col(t) + lane_base;
+  const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(t) * L::O_STRIDE + lane_base;
   const float c = p.scale_log2;
   const bool causal = (p.mask_kind & ATTN_MASK_CAUSAL_BIT) != 0;
   const bool padding = (p.mask_kind & ATTN_MASK_PADDING_BIT) != 0;
@@ -428,6 +467,11 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
       reg_fence(rb);
       reg_fence(rc);
       reg_fence(rd);
+      if constexpr (L::EARLY_S) {
+        // S_t(j) is in registers: its columns may take S_t(j+1)
+        tc_fence_before();
+        mbar_arrive(&bars[L::B_S_EMPTY + t]);
+      }
       float s[128];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -455,9 +499,19 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
       const float m_tile = mx * c;  // scale > 0, so the max commutes with it
       const float m_new = fmaxf(m, m_tile);
       const bool need = m_new > m + ATTN_RESCALE_THRESHOLD;
+      if (L::EARLY_S && j > 0) {
+        // S_t(j) was issued before P_t(j-1) V, so its commit does not cover
+        // that MMA: wait for it before O is rescaled or P_t(j) overwrites
+        // the P columns it reads
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&bars[L::B_PV_DONE + t], (s_cnt - 2u) & 1u, ctl));
+        if (!ok) break;
+        tc_fence_after();
+      }
       if (__any_sync(0xffffffffu, need && j > 0)) {
         // rescale this row's O accumulator.  P_t(j-1) V has completed: the
-        // commit that signalled S_t(j) covers every earlier MMA of the issuer.
+        // commit that signalled S_t(j) covers every earlier MMA of the issuer
+        // (early-S: the wait above).
         const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
         const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
@@ -595,6 +649,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       mbar_init(&bars[L::B_S_FULL + t], 1);
       mbar_init(&bars[L::B_P_FULL + t], 128);
       mbar_init(&bars[L::B_O_DONE + t], 1);
+      mbar_init(&bars[L::B_S_EMPTY + t], 128);
+      mbar_init(&bars[L::B_PV_DONE + t], 1);
     }
     for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(&bars[L::B_K_FULL + s], 1);
