@@ -21,12 +21,14 @@ def _gemm_case(M, N, K, seed):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 192), (384, 768, 1024),
-                                   (1024, 3072, 1024)])
+                                   (640, 256, 64), (1024, 3072, 1024), (8192, 4096, 512)])
 def test_gemm_matches_fp64_matmul(cuda_lib, M, N, K):
     """C = A B: bf16 inputs, fp32 accumulation, one bf16 rounding of the
     result.  The fp64 product of the same bf16 values (a library matmul) is
     the reference; the bound is half a bf16 ulp (2^-8 relative) plus fp32
-    accumulation slack."""
+    accumulation slack.  The shapes cover a pair whose second 128 rows lie
+    past M (M = 128, 384, 640) and, at 8192 x 4096, several 256 x 256 tiles
+    per CTA pair, so both TMEM accumulators are reused."""
     a, b = _gemm_case(M, N, K, seed=M + N + K)
     C = down(cuda_lib.gemm_bf16(up(a), up(b)))
     cuda_lib.check_device_status()

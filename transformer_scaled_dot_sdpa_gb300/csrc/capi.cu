@@ -37,6 +37,7 @@ struct DeviceState {
   unsigned int* status = nullptr;
   bool attn_attr[4] = {false, false, false, false};
   bool gemm_attr = false;
+  int gemm_pairs = 0;  // CTA pairs of the GEMM kernel resident at once
   void* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch
 };
 
@@ -218,14 +219,27 @@ attn_status_t map_2d(CUtensorMap* m, const void* base, int rows, int cols, int c
 // C[M,N] = A[M,K] B[K,N]; sizes already validated.
 attn_status_t run_gemm(DeviceState* ds, const void* A, const void* Bm, void* C, int M, int N,
                        int K, cudaStream_t stream) {
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mc;
   attn_status_t st;
-  if ((st = map_2d(&ma, A, M, K, gb300::GEMM_BK, gb300::GEMM_BM)) != ATTN_OK) return st;
+  if ((st = map_2d(&ma, A, M, K, gb300::GEMM_BK, gb300::GEMM_BM_CTA)) != ATTN_OK) return st;
   if ((st = map_2d(&mb, Bm, K, N, 64, gb300::GEMM_BK)) != ATTN_OK) return st;
+  if ((st = map_2d(&mc, C, M, N, 64, 32)) != ATTN_OK) return st;  // epilogue store boxes
   if (!ds->gemm_attr) {
     if (cudaFuncSetAttribute(gb300::gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              gb300::GemmLayout::SMEM_BYTES) != cudaSuccess)
       return ATTN_ERR_CUDA;
+    // The kernel is persistent: launch only as many pairs as can be resident
+    // together (a TPC with one SM enabled cannot host a pair).
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(static_cast<unsigned>(ds->num_sms & ~1), 1, 1);
+    cfg.blockDim = dim3(gb300::GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = gb300::GemmLayout::SMEM_BYTES;  // cluster size: the kernel's own (2)
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gb300::gemm_bf16_kernel, &cfg) != cudaSuccess ||
+        clusters < 1)
+      return ATTN_ERR_CUDA;
+    ds->gemm_pairs = clusters;
     ds->gemm_attr = true;
   }
   gb300::GemmParams p;
@@ -233,7 +247,7 @@ attn_status_t run_gemm(DeviceState* ds, const void* A, const void* Bm, void* C, 
   p.M = M;
   p.N = N;
   p.K = K;
-  p.m_tiles = M / gb300::GEMM_BM;
+  p.m_tiles = (M + gb300::GEMM_BM - 1) / gb300::GEMM_BM;
   p.n_tiles = N / gb300::GEMM_BN;
   p.k_blocks = K / gb300::GEMM_BK;
   p.C = static_cast<__nv_bfloat16*>(C);
@@ -243,9 +257,9 @@ attn_status_t run_gemm(DeviceState* ds, const void* A, const void* Bm, void* C, 
     p.wait_limit_ns = g_wait_limit_ns;
   }
   const int tiles = p.m_tiles * p.n_tiles;
-  const int grid = tiles < ds->num_sms ? tiles : ds->num_sms;
-  gb300::gemm_bf16_kernel<<<grid, gb300::GEMM_THREADS, gb300::GemmLayout::SMEM_BYTES, stream>>>(
-      ma, mb, p);
+  const int pairs = tiles < ds->gemm_pairs ? tiles : ds->gemm_pairs;
+  gb300::gemm_bf16_kernel<<<2 * pairs, gb300::GEMM_THREADS, gb300::GemmLayout::SMEM_BYTES,
+                            stream>>>(ma, mb, mc, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -535,7 +549,7 @@ size_t mha_layer_workspace_bytes(int B, int L, int d_model, int h) {
 attn_status_t attn_gemm_bf16(const void* A, const void* Bm, void* C, int M, int N, int K,
                              void* stream) {
   if (M < 0 || N < 0 || K < 0) return ATTN_ERR_INVALID_ARG;
-  if (M % gb300::GEMM_BM != 0 || N % gb300::GEMM_BN != 0 || K % gb300::GEMM_BK != 0)
+  if (M % gb300::GEMM_BM_CTA != 0 || N % gb300::GEMM_BN != 0 || K % gb300::GEMM_BK != 0)
     return ATTN_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return ATTN_OK;
   if (K == 0) return ATTN_ERR_UNSUPPORTED;
@@ -562,7 +576,7 @@ attn_status_t mha_layer_fwd(const void* X, const void* W_QKV, const void* W_O, i
   if (dk != 64 && dk != 128) return ATTN_ERR_UNSUPPORTED;
   if (d_model % gb300::GEMM_BN != 0) return ATTN_ERR_UNSUPPORTED;
   const long long rows = static_cast<long long>(B) * L;
-  if (rows % gb300::GEMM_BM != 0 || rows >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  if (rows % gb300::GEMM_BM_CTA != 0 || rows >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
   if (rows == 0) return ATTN_OK;
   if (!X || !W_QKV || !W_O || !Y || !workspace) return ATTN_ERR_INVALID_ARG;
   if ((mask_kind & ATTN_MASK_PADDING) && !kv_lens) return ATTN_ERR_INVALID_ARG;

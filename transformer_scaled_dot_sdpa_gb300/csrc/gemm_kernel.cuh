@@ -5,14 +5,8 @@
 // projection Concat(heads) W_O.
 //
 //   A [M, K] row-major (K-major operand), B [K, N] row-major (N-major operand),
-//   C [M, N] row-major.  Tiles of 128 x 256, K blocks of 64.
-//
-// CTA organisation (persistent, one CTA per SM):
-//   warp 0      TMA producer (one thread): A and B tiles into a 4-stage ring
-//   warp 1      MMA issuer (whole warp, one elected lane issues) + TMEM
-//               owner; two 256-column fp32 accumulators so the epilogue of
-//               one tile overlaps the main loop of the next
-//   warps 2-5   epilogue: TMEM -> registers -> bf16 -> global, one row each
+//   C [M, N] row-major.  Tiles of 256 x 256 computed by a pair of CTAs with
+//   the two-SM form of tcgen05.mma (cta_group::2), K blocks of 64.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -21,30 +15,35 @@
 
 namespace gb300 {
 
-constexpr int GEMM_BM = 128;
-constexpr int GEMM_BN = 256;
+constexpr int GEMM_BM = 256;        // rows of a tile: 128 in each CTA of the pair
+constexpr int GEMM_BM_CTA = 128;
+constexpr int GEMM_BN = 256;        // columns of a tile: B split 128 / 128 over the pair
+constexpr int GEMM_BN_CTA = 128;
 constexpr int GEMM_BK = 64;
-constexpr int GEMM_STAGES = 4;
+constexpr int GEMM_STAGES = 6;
 constexpr int GEMM_THREADS = 192;
 constexpr uint32_t GEMM_TMEM_COLS = 512;
 enum : unsigned int { GEMM_STATUS_TIMEOUT = 1u };
 
 struct GemmLayout {
-  static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;        // 16 KB
+  static constexpr int A_BYTES = GEMM_BM_CTA * GEMM_BK * 2;    // 16 KB: this CTA's 128 rows
   static constexpr int B_CHUNK = GEMM_BK * 64 * 2;             // 64 K-rows x 64 N = 8 KB
-  static constexpr int B_BYTES = GEMM_BK * GEMM_BN * 2;        // 32 KB
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int B_BYTES = GEMM_BK * GEMM_BN_CTA * 2;    // 16 KB: this CTA's 128 columns
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;        // per CTA
+  static constexpr int C_BOX_BYTES = 32 * 64 * 2;              // 32 rows x 64 columns of C
   static constexpr int A_OFF = 0;
   static constexpr int B_OFF = GEMM_STAGES * A_BYTES;
-  static constexpr int BAR_OFF = B_OFF + GEMM_STAGES * B_BYTES;
-  static constexpr int B_FULL = 0;
-  static constexpr int B_EMPTY = GEMM_STAGES;
-  static constexpr int B_ACC_FULL = 2 * GEMM_STAGES;
-  static constexpr int B_ACC_EMPTY = B_ACC_FULL + 2;
+  static constexpr int C_OFF = B_OFF + GEMM_STAGES * B_BYTES;  // 2 staging boxes per epilogue warp
+  static constexpr int BAR_OFF = C_OFF + 4 * 2 * C_BOX_BYTES;
+  static constexpr int B_FULL = 0;                       // used in the even CTA
+  static constexpr int B_EMPTY = GEMM_STAGES;            // both CTAs
+  static constexpr int B_ACC_FULL = 2 * GEMM_STAGES;     // both CTAs
+  static constexpr int B_ACC_EMPTY = B_ACC_FULL + 2;     // used in the even CTA
   static constexpr int B_DRAIN = B_ACC_EMPTY + 2;
   static constexpr int N_BARS = B_DRAIN + 1;
   static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
 };
 
 struct GemmParams {
@@ -62,9 +61,30 @@ __device__ __forceinline__ void gemm_tile_coords(const GemmParams& p, int tile, 
   n0 = nt * GEMM_BN;
 }
 
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+// One cluster = one pair of CTAs on a TPC; the pair computes 256 x 256 output
+// tiles, persistent over the tile list.  Per CTA of the pair:
+//   warp 0      TMA producer (one thread): its 128 rows of A and its 128
+//               columns of B into a 6-stage ring; the completion of both
+//               CTAs' loads is counted on the even CTA's full-barrier
+//   warp 1      TMEM (both CTAs allocate the pair's 512 columns together);
+//               in the even CTA also the MMA issuer (whole warp, one elected
+//               lane issues tcgen05.mma.cta_group::2 with M = N = 256; its
+//               commits arrive on the barriers of both CTAs)
+//   warps 2-5   epilogue of this CTA's 128 rows: TMEM -> bf16 -> a 128B-
+//               swizzled staging box of 32 rows x 64 columns per warp (two,
+//               alternating) -> TMA tensor store; the four warps of each CTA
+//               release an accumulator with one arrival each on the even
+//               CTA's accumulator-empty barrier
+// Row-per-thread global stores here (32 scattered 16-byte pieces per warp
+// instruction) held up the TMA loads and the MMAs of the next tile; the TMA
+// store writes whole 128-byte lines.
+// Per SM and 64-deep K block the tensor core reads 32 KB of operands from
+// shared memory for 2 x 128 x 256 x 64 FLOPs, two thirds of what a one-CTA
+// 128 x 256 tile needs.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   using L = GemmLayout;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -74,111 +94,132 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31u);
+  const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: its peer
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int n_pairs = static_cast<int>(gridDim.x >> 1);
   const int n_tiles_total = p.m_tiles * p.n_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < GEMM_STAGES; ++s) {
-      mbar_init(&bars[L::B_FULL + s], 1);
-      mbar_init(&bars[L::B_EMPTY + s], 1);
+      mbar_init(&bars[L::B_FULL + s], 1);    // the even CTA's producer arrives (+ both CTAs' bytes)
+      mbar_init(&bars[L::B_EMPTY + s], 1);   // one multicast commit
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(&bars[L::B_ACC_FULL + a], 1);
-      mbar_init(&bars[L::B_ACC_EMPTY + a], 128);
+      mbar_init(&bars[L::B_ACC_FULL + a], 1);  // one multicast commit
+      mbar_init(&bars[L::B_ACC_EMPTY + a], 8);  // 4 epilogue warps x 2 CTAs
     }
     mbar_init(&bars[L::B_DRAIN], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, GEMM_TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, GEMM_TMEM_COLS);
+    tmem_relinquish_pair();
   }
+  // both CTAs' barriers are initialised and the pair's TMEM is allocated
+  // before either CTA signals the other
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns, GEMM_STATUS_TIMEOUT};
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer (both CTAs) ----------------
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      const uint32_t full0 = mapa_shared(smem_u32(&bars[L::B_FULL]), 0u);
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x) {
+      for (int tile = pair; ok && tile < n_tiles_total; tile += n_pairs) {
         int m0, n0;
         gemm_tile_coords(p, tile, m0, n0);
+        const int row = m0 + static_cast<int>(rank) * GEMM_BM_CTA;
+        const int col = n0 + static_cast<int>(rank) * GEMM_BN_CTA;
         for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
           const int s = static_cast<int>(it % GEMM_STAGES);
           if (it >= static_cast<uint32_t>(GEMM_STAGES)) {
             ok = mbar_wait(&bars[L::B_EMPTY + s], ((it / GEMM_STAGES) - 1u) & 1u, ctl);
             if (!ok) break;
           }
-          mbar_arrive_expect_tx(&bars[L::B_FULL + s], L::STAGE_BYTES);
-          tma_load_2d(smem + L::A_OFF + s * L::A_BYTES, &tmA, &bars[L::B_FULL + s],
-                      kb * GEMM_BK, m0);
+          // the even CTA's full-barrier counts the bytes of both CTAs; the
+          // odd CTA's bytes may land before this expect_tx (the count then
+          // runs below zero until it does, and the phase cannot complete
+          // without this arrival)
+          if (rank == 0) mbar_arrive_expect_tx(&bars[L::B_FULL + s], 2 * L::STAGE_BYTES);
+          const uint32_t fb = full0 + static_cast<uint32_t>(s) * 8u;
+          tma_load_2d_pair(smem + L::A_OFF + s * L::A_BYTES, &tmA, fb, kb * GEMM_BK, row);
 #pragma unroll
-          for (int c = 0; c < GEMM_BN / 64; ++c)
-            tma_load_2d(smem + L::B_OFF + s * L::B_BYTES + c * L::B_CHUNK, &tmB,
-                        &bars[L::B_FULL + s], n0 + 64 * c, kb * GEMM_BK);
+          for (int c = 0; c < GEMM_BN_CTA / 64; ++c)
+            tma_load_2d_pair(smem + L::B_OFF + s * L::B_BYTES + c * L::B_CHUNK, &tmB, fb,
+                             col + 64 * c, kb * GEMM_BK);
         }
       }
+      // Unwind: every commit that arrives on this CTA's empty-barriers, and
+      // (even CTA) the loads of both CTAs, must have landed before the pair
+      // leaves; on the normal path these phases completed long ago.
       for (int s = 0; s < GEMM_STAGES; ++s) {
         if (it <= static_cast<uint32_t>(s)) continue;
         const uint32_t n_s = (it - s + GEMM_STAGES - 1) / GEMM_STAGES;
-        mbar_wait_drain(&bars[L::B_FULL + s], (n_s - 1u) & 1u, ctl.limit_ns);
+        if (rank == 0) mbar_wait_drain(&bars[L::B_FULL + s], (n_s - 1u) & 1u, ctl.limit_ns);
+        mbar_wait_drain(&bars[L::B_EMPTY + s], (n_s - 1u) & 1u, ctl.limit_ns);
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    // The whole warp waits and computes operands; one elected lane issues,
-    // so the operands stay warp-uniform and each MMA issues quickly.
-    constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, GEMM_BN, true);
-    constexpr unsigned FULL = 0xffffffffu;
-    const uint64_t a_desc = smem_desc_sw128(smem_u32(smem + L::A_OFF), 16, 1024);
-    const uint64_t b_desc = smem_desc_sw128(smem_u32(smem + L::B_OFF), L::B_CHUNK, 1024);
-    uint32_t it = 0, tcount = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x, ++tcount) {
-      const uint32_t acc = tcount & 1u;
-      if (tcount >= 2u) {
-        ok = __all_sync(FULL, mbar_wait(&bars[L::B_ACC_EMPTY + acc], ((tcount >> 1) - 1u) & 1u, ctl));
-        if (!ok) break;
-        tc_fence_after();
-      }
-      const uint32_t d_tmem = tmem + acc * GEMM_BN;
-      for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
-        const int s = static_cast<int>(it % GEMM_STAGES);
-        ok = __all_sync(FULL, mbar_wait(&bars[L::B_FULL + s], (it / GEMM_STAGES) & 1u, ctl));
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t ad = a_desc + static_cast<uint64_t>((s * L::A_BYTES) >> 4);
-        const uint64_t bd = b_desc + static_cast<uint64_t>((s * L::B_BYTES) >> 4);
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < GEMM_BK / 16; ++kk)
-            mma_bf16_ss(d_tmem, ad + static_cast<uint64_t>((kk * 32) >> 4),
-                        bd + static_cast<uint64_t>((kk * 2048) >> 4), IDESC,
-                        (kb > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars[L::B_EMPTY + s]);
+    if (rank == 0) {
+      // ---------------- MMA issuer (even CTA) ----------------
+      // The whole warp waits and computes operands; one elected lane issues,
+      // so the operands stay warp-uniform and each MMA issues quickly.
+      constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, GEMM_BN, true);
+      constexpr unsigned FULL = 0xffffffffu;
+      constexpr uint16_t BOTH = 0x3;
+      const uint64_t a_desc = smem_desc_sw128(smem_u32(smem + L::A_OFF), 16, 1024);
+      const uint64_t b_desc = smem_desc_sw128(smem_u32(smem + L::B_OFF), L::B_CHUNK, 1024);
+      uint32_t it = 0, tcount = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < n_tiles_total; tile += n_pairs, ++tcount) {
+        const uint32_t acc = tcount & 1u;
+        if (tcount >= 2u) {
+          ok = __all_sync(FULL, mbar_wait(&bars[L::B_ACC_EMPTY + acc], ((tcount >> 1) - 1u) & 1u, ctl));
+          if (!ok) break;
+          tc_fence_after();
         }
+        const uint32_t d_tmem = tmem + acc * GEMM_BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+          const int s = static_cast<int>(it % GEMM_STAGES);
+          ok = __all_sync(FULL, mbar_wait(&bars[L::B_FULL + s], (it / GEMM_STAGES) & 1u, ctl));
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t ad = a_desc + static_cast<uint64_t>((s * L::A_BYTES) >> 4);
+          const uint64_t bd = b_desc + static_cast<uint64_t>((s * L::B_BYTES) >> 4);
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < GEMM_BK / 16; ++kk)
+              mma_bf16_ss_pair(d_tmem, ad + static_cast<uint64_t>((kk * 32) >> 4),
+                               bd + static_cast<uint64_t>((kk * 2048) >> 4), IDESC,
+                               (kb > 0 || kk > 0) ? 1u : 0u);
+            mma_commit_pair_multicast(&bars[L::B_EMPTY + s], BOTH);
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (elect_one()) mma_commit_pair_multicast(&bars[L::B_ACC_FULL + acc], BOTH);
         __syncwarp();
       }
-      if (!ok) break;
-      if (elect_one()) mma_commit(&bars[L::B_ACC_FULL + acc]);
+      if (elect_one()) mma_commit_pair(&bars[L::B_DRAIN]);
       __syncwarp();
+      mbar_wait_drain(&bars[L::B_DRAIN], 0u, ctl.limit_ns);
     }
-    if (elect_one()) mma_commit(&bars[L::B_DRAIN]);
-    __syncwarp();
-    mbar_wait_drain(&bars[L::B_DRAIN], 0u, ctl.limit_ns);
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
-    const int row = static_cast<int>((warp & 3) * 32 + lane);  // TMEM lane = tile row
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t tcount = 0;
+    // ---------------- epilogue (warps 2..5, both CTAs) ----------------
+    const int wq = warp & 3;  // TMEM lane quarter = rows 32 wq .. 32 wq + 31 of this CTA
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(&bars[L::B_ACC_EMPTY]), 0u);
+    uint8_t* stage = smem + L::C_OFF + wq * 2 * L::C_BOX_BYTES;
+    uint32_t tcount = 0, n_stores = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x, ++tcount) {
+    for (int tile = pair; tile < n_tiles_total; tile += n_pairs, ++tcount) {
       const uint32_t acc = tcount & 1u;
       ok = mbar_wait(&bars[L::B_ACC_FULL + acc], (tcount >> 1) & 1u, ctl);
       ok = __all_sync(0xffffffffu, ok);
@@ -186,31 +227,57 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tc_fence_after();
       int m0, n0;
       gemm_tile_coords(p, tile, m0, n0);
-      __nv_bfloat16* crow = p.C + static_cast<long long>(m0 + row) * p.N + n0;
+      const int box_row = m0 + static_cast<int>(rank) * GEMM_BM_CTA + wq * 32;
+      // M is a multiple of 128: a box of 32 rows lies wholly inside or past M
+      const bool rows_in = box_row < p.M;
 #pragma unroll 1
-      for (int cc = 0; cc < GEMM_BN / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem + acc * GEMM_BN + lane_base + cc * 32u, r);
-        tmem_ld_wait(r);
-        uint32_t w[16];
+      for (int c = 0; c < GEMM_BN / 64; ++c) {
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(tmem + acc * GEMM_BN + lane_base + c * 64u, r0);
+        tmem_ld_32x32b_x32(tmem + acc * GEMM_BN + lane_base + c * 64u + 32u, r1);
+        tmem_ld_wait(r0);
+        reg_fence(r1);
+        if (rows_in) {
+          uint8_t* box = stage + (n_stores & 1u) * L::C_BOX_BYTES;
+          // the store issued two boxes ago has finished reading this buffer
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+          // row `lane` of the box: 8 pieces of 16 bytes, piece j at position
+          // j ^ (row % 8) (the 128-byte swizzle of the tensor map)
+          const uint32_t row_addr = smem_u32(box) + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          st_global_v4(crow + cc * 32 + i * 8, w[4 * i], w[4 * i + 1], w[4 * i + 2],
-                       w[4 * i + 3]);
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t* q = (j < 4) ? &r0[8 * j] : &r1[8 * (j - 4)];
+            st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
+                         pack_bf16x2(__uint_as_float(q[0]), __uint_as_float(q[1])),
+                         pack_bf16x2(__uint_as_float(q[2]), __uint_as_float(q[3])),
+                         pack_bf16x2(__uint_as_float(q[4]), __uint_as_float(q[5])),
+                         pack_bf16x2(__uint_as_float(q[6]), __uint_as_float(q[7])));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, box, n0 + 64 * c, box_row);
+            bulk_commit_group();
+          }
+          ++n_stores;
+        }
       }
       tc_fence_before();
-      mbar_arrive(&bars[L::B_ACC_EMPTY + acc]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty0 + acc * 8u);
     }
+    // the stores have read their boxes and written C before the CTA leaves
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
   }
 
+  // Neither CTA leaves (or frees TMEM) while the other may still signal it.
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, GEMM_TMEM_COLS);
+    tmem_dealloc_pair(tmem, GEMM_TMEM_COLS);
   }
 }
 
