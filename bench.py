@@ -41,6 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # sources whose hash a committed DRAM-traffic figure is tied to, per kernel
 KERNEL_SOURCES = {
     "attn_fwd_kernel": ["attn_fwd_kernel.cuh", "ptx.cuh"],
+    "gemm_bf16_kernel": ["gemm_kernel.cuh", "ptx.cuh"],
     "attn_fwd_split_kernel": ["attn_fwd_split_kernel.cuh", "attn_fwd_kernel.cuh", "ptx.cuh"],
 }
 
@@ -610,11 +611,13 @@ def layer_arm(args, w):
               "wo_gemm": (2.0 * N * dm * dm, ms_wo)}
     dom = max(stages, key=lambda k: stages[k][1])
     achieved = stages[dom][0] / (stages[dom][1] * 1e-3) / 1e12
+    kernel = {"qkv_gemm": "gemm_bf16_kernel", "wo_gemm": "gemm_bf16_kernel",
+              "attention": attention_kernel_name(w.B, w.H, w.L, dk)}[dom]
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": profiled_traffic(w.name, kernel) if dom == "attention" else None,
                 "peak_source": "%s (bf16 dense burst)" % peak_src,
-                "kernel": {"qkv_gemm": "gemm_bf16_kernel", "wo_gemm": "gemm_bf16_kernel",
-                           "attention": attention_kernel_name(w.B, w.H, w.L, dk)}[dom],
+                "kernel": kernel,
                 "stages_ms": {k: v[1] for k, v in stages.items()},
                 "stages_tflops": {k: v[0] / (v[1] * 1e-3) / 1e12 for k, v in stages.items()}}
     cpu = None
