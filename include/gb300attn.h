@@ -112,6 +112,49 @@ attn_status_t attn_fwd_gqa(const void* Q, const void* K, const void* V, int B, i
                            void* stream);
 
 /*
+ * attn_fwd_host -- attn_fwd_gqa with Q, K, V, O, LSE and kv_lens in HOST
+ * memory.  The call copies the inputs to the device, runs the attention
+ * kernels and copies the results back, overlapping the three.  The work is
+ * cut into up to 16 chunks of at least 8 MB, each either whole batch
+ * elements or a group of K/V heads of one element with their query heads, so
+ * each chunk's Q, K, V, O and LSE are contiguous and the chunks carry equal
+ * work.  A chunk's inputs are copied while earlier chunks compute, and its O
+ * and LSE are copied back as soon as it is done.  Each (b, head) runs the
+ * work items of attn_fwd_gqa: with ATTN_SCHEDULE_TWO_QTILES every element is
+ * bit-identical to it.  ATTN_SCHEDULE_SPLIT_KEYS deals an item's key tiles
+ * to its two softmax groups by the CTA's running tile count, so there a row
+ * may be summed in the other order (a difference of rounding).
+ *
+ *   Q, K, V, O, LSE, kv_lens   host pointers, layouts as for attn_fwd_gqa;
+ *               page-locked memory (cudaHostAlloc / cudaHostRegister) lets
+ *               the copies run asynchronously and overlap; pageable memory
+ *               works but is copied synchronously.  LSE may be NULL.
+ *   workspace   device scratch of at least attn_fwd_host_workspace_bytes(...)
+ *               bytes, 256-byte aligned, owned by the caller; it receives
+ *               device copies of Q, K, V, O, LSE and kv_lens.  Calls that
+ *               share it must not overlap.
+ *   stream      the call's work runs on internal streams of the library that
+ *               start after the work already queued on `stream`; `stream`
+ *               is made to wait for all of it.  The host buffers must stay
+ *               valid, and O / LSE must not be read, until `stream` has been
+ *               synchronised.
+ *
+ * Errors as for attn_fwd_gqa, plus ATTN_ERR_INVALID_ARG for a missing or
+ * too-small workspace and ATTN_ERR_MISALIGNED for a workspace not 256-byte
+ * aligned.
+ */
+attn_status_t attn_fwd_host(const void* Q, const void* K, const void* V, int B, int h, int h_kv,
+                            int Lq, int Lk, int d_k, int d_v, int mask_kind,
+                            const int32_t* kv_lens, float scale, void* O, float* LSE,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_fwd_host_workspace_bytes -- device scratch attn_fwd_host needs for
+ * these sizes; 0 for unsupported sizes.
+ */
+size_t attn_fwd_host_workspace_bytes(int B, int h, int h_kv, int Lq, int Lk, int d_k, int d_v);
+
+/*
  * attn_decode -- attn_fwd_gqa for few query rows against a long key/value
  * cache (decoding: the Lq new tokens are the last Lq of each sequence, so the
  * usual mask is ATTN_MASK_CAUSAL_BOTTOM_RIGHT, with kv_lens for caches of

@@ -161,3 +161,33 @@ def test_probe_ex2_validation(cdll):
             (1, 1024, 1, None, dummy),      # NULL cycles
             (1, 1024, 1, dummy, None)]:     # NULL sink
         assert f(blocks, threads, iters, cyc, sink, None) == 1
+
+
+def test_host_entry_validation(cdll):
+    """attn_fwd_host rejects a missing, short or misaligned workspace before
+    any CUDA call; its size is the sum of the device copies, 256-aligned."""
+    f = cdll.attn_fwd_host
+    f.restype = ctypes.c_int
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [vp, vp, vp] + [i32] * 8 + [vp, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp]
+    ws = cdll.attn_fwd_host_workspace_bytes
+    ws.restype = ctypes.c_size_t
+    ws.argtypes = [i32] * 7
+    B, h, hkv, Lq, Lk, d = 2, 8, 2, 1000, 3000, 64
+    def r256(x):
+        return (x + 255) // 256 * 256
+    want = (r256(B * h * Lq * d * 2) + 2 * r256(B * hkv * Lk * d * 2) + r256(B * h * Lq * d * 2)
+            + r256(B * h * Lq * 4) + r256(B * 4))
+    assert ws(B, h, hkv, Lq, Lk, d, d) == want
+    assert ws(B, h, hkv, Lq, Lk, 96, 96) == 0        # unsupported head size
+    assert ws(B, h, 3, Lq, Lk, d, d) == 0            # h not a multiple of h_kv
+    host = (ctypes.c_uint8 * 64)()
+    p = ctypes.cast(host, vp)
+    def call(work, nbytes):
+        return f(p, p, p, B, h, hkv, Lq, Lk, d, d, 0, None, 0.0, p, None, work, nbytes, None)
+    assert call(None, want) == 1                     # no workspace
+    assert call(ctypes.c_void_p(1 << 20), want - 256) == 1   # too small
+    assert call(ctypes.c_void_p((1 << 20) + 16), want) == 3  # not 256-byte aligned
+    # padding mask without kv_lens
+    assert f(p, p, p, B, h, hkv, Lq, Lk, d, d, 2, None, 0.0, p, None, ctypes.c_void_p(1 << 20),
+             want, None) == 1

@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "MASK_NONE", "MASK_CAUSAL", "MASK_PADDING", "MASK_CAUSAL_BOTTOM_RIGHT", "AttnError", "attn_fwd",
-    "attn_decode", "attn_decode_workspace_bytes",
+    "attn_fwd_host", "attn_fwd_host_workspace_bytes", "attn_decode", "attn_decode_workspace_bytes",
     "attn_weights", "mha_layer_fwd",
     "mha_layer_workspace_bytes", "mha_layer_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gemm_bf16",
     "check_device_status", "set_wait_limit_ns", "set_schedule", "SCHEDULE_AUTO",
@@ -68,6 +68,11 @@ def _load():
     L.attn_fwd_gqa.restype = i32
     L.attn_fwd_gqa.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp,
                                vp, vp]
+    L.attn_fwd_host.restype = i32
+    L.attn_fwd_host.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp,
+                                vp, sz, vp]
+    L.attn_fwd_host_workspace_bytes.restype = sz
+    L.attn_fwd_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     L.attn_decode.restype = i32
     L.attn_decode.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp, vp, sz,
                               vp]
@@ -166,6 +171,56 @@ def attn_fwd(q, k, v, mask_kind=MASK_NONE, kv_lens=None, scale=None, out=None, l
 
 def attn_decode_workspace_bytes(B, h, h_kv, Lq, Lk, d):
     return int(lib.attn_decode_workspace_bytes(B, h, h_kv, Lq, Lk, d))
+
+
+def _host_tensor(t, name, dtype):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError("%s must be a CPU tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def attn_fwd_host_workspace_bytes(B, h, h_kv, Lq, Lk, d_k, d_v=None):
+    return int(lib.attn_fwd_host_workspace_bytes(int(B), int(h), int(h_kv), int(Lq), int(Lk),
+                                                 int(d_k), int(d_v if d_v is not None else d_k)))
+
+
+def attn_fwd_host(q, k, v, mask_kind=MASK_NONE, kv_lens=None, scale=None, out=None, lse=None,
+                  return_lse=True, workspace=None, stream=None):
+    """attn_fwd on host (CPU) tensors: the library copies them to the device,
+    computes and copies O / LSE back, overlapping copies and kernels over
+    chunks of heads.  q/k/v/out/lse are CPU tensors (pinned for overlap),
+    ``kv_lens`` an int32 CPU tensor, ``workspace`` a uint8 CUDA tensor
+    (allocated when not given).  The results are valid once ``stream`` (the
+    current stream by default) has been synchronised."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _host_tensor(t, n, torch.bfloat16)
+    B, h, Lq, dk = q.shape
+    h_kv, Lk, dv = k.shape[1], k.shape[2], v.shape[3]
+    if tuple(k.shape) != (B, h_kv, Lk, dk) or tuple(v.shape) != (B, h_kv, Lk, dv):
+        raise ValueError("q/k/v shapes do not match")
+    if out is None:
+        out = torch.empty((B, h, Lq, dv), dtype=torch.bfloat16).pin_memory()
+    _host_tensor(out, "out", torch.bfloat16)
+    if tuple(out.shape) != (B, h, Lq, dv):
+        raise ValueError("out has the wrong shape")
+    if lse is None and return_lse:
+        lse = torch.empty((B, h, Lq), dtype=torch.float32).pin_memory()
+    if lse is not None:
+        _host_tensor(lse, "lse", torch.float32)
+    if kv_lens is not None:
+        _host_tensor(kv_lens, "kv_lens", torch.int32)
+    need = attn_fwd_host_workspace_bytes(B, h, h_kv, Lq, Lk, dk, dv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    _dev_tensor(workspace, "workspace", torch.uint8)
+    st = lib.attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), B, h, h_kv, Lq, Lk, dk, dv, int(mask_kind),
+                           _ptr(kv_lens), float(scale) if scale else 0.0, _ptr(out), _ptr(lse),
+                           _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(st, "attn_fwd_host")
+    return out, lse
 
 
 def attn_decode(q, k, v, mask_kind=MASK_CAUSAL_BOTTOM_RIGHT, kv_lens=None, scale=None, out=None,

@@ -38,10 +38,15 @@ struct DeviceState {
   bool attn_attr[4] = {false, false, false, false};
   bool gemm_attr = false;
   int gemm_pairs = 0;  // CTA pairs of the GEMM kernel resident at once
+  // attn_fwd_host: copy-in, copy-out and a second compute stream, and the
+  // events that order them (created on first use)
+  cudaStream_t host_in = nullptr, host_out = nullptr, host_comp = nullptr;
+  cudaEvent_t host_ev[2 * 16 + 2] = {};
   void* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch
 };
 
 std::mutex g_mutex;
+std::mutex g_host_mutex;  // one attn_fwd_host enqueue at a time (shared events)
 DeviceState g_dev[kMaxDevices];
 unsigned long long g_wait_limit_ns = kDefaultWaitLimitNs;
 long long g_debug_skip_kv_load = -1;
@@ -317,11 +322,14 @@ attn_status_t attn_fwd(const void* Q, const void* K, const void* V, int B, int h
                       stream);
 }
 
-attn_status_t attn_fwd_gqa(const void* Q, const void* K, const void* V, int B, int h, int h_kv,
-                           int Lq, int Lk, int d_k, int d_v, int mask_kind,
-                           const int32_t* kv_lens, float scale, void* O, float* LSE,
-                           void* stream) {
-  // ---- host-side validation (no CUDA call before this point) ----
+}  // extern "C"
+
+namespace {
+
+// Checks shared by attn_fwd_gqa and attn_fwd_host on everything but the
+// pointers (no CUDA call).
+attn_status_t check_attn_shape(int B, int h, int h_kv, int Lq, int Lk, int d_k, int d_v,
+                               int mask_kind, float scale) {
   if (B < 0 || h < 0 || Lq < 0 || Lk < 0) return ATTN_ERR_INVALID_ARG;
   if (h_kv < 1 || (h > 0 && h % h_kv != 0)) return ATTN_ERR_INVALID_ARG;
   if ((mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_PADDING | ATTN_MASK_CAUSAL_BOTTOM_RIGHT)) != 0)
@@ -334,6 +342,77 @@ attn_status_t attn_fwd_gqa(const void* Q, const void* K, const void* V, int B, i
   // work items of the finer schedule (128 query rows each) must fit an int
   const long long n_qblocks = (static_cast<long long>(Lq) + gb300::SPLIT_ROWS - 1) / gb300::SPLIT_ROWS;
   if (static_cast<long long>(B) * h * n_qblocks >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+// Attention over contiguous [B, h, L, d] device buffers.
+attn_status_t attn_device(DeviceState* ds, const void* Q, const void* K, const void* V, int B,
+                          int h, int h_kv, int Lq, int Lk, int d, int mask_kind,
+                          const int32_t* kv_lens, float scale, void* O, float* LSE,
+                          cudaStream_t s) {
+  const long long osl = d, osh = static_cast<long long>(Lq) * d, osb = osh * h;
+  attn_status_t st;
+  CUtensorMap mq, mk, mv;
+  if ((st = map_bhld(&mq, Q, B, h, Lq, d)) != ATTN_OK) return st;
+  if ((st = map_bhld(&mk, K, B, h_kv, Lk, d)) != ATTN_OK) return st;
+  if ((st = map_bhld(&mv, V, B, h_kv, Lk, d)) != ATTN_OK) return st;
+  return run_attention(ds, mq, mk, mv, 0, B, h, h_kv, Lq, Lk, d, mask_kind, kv_lens, scale, O,
+                       osb, osh, osl, LSE, s);
+}
+
+// attn_fwd_host: where the device copies of Q, K, V, O, LSE and kv_lens live
+// in the caller's workspace (byte offsets, 256-aligned).
+struct HostLayout {
+  size_t q, k, v, o, lse, kv, total;
+};
+constexpr int kHostMaxChunks = 16;
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+HostLayout host_layout(int B, int h, int h_kv, int Lq, int Lk, int d) {
+  HostLayout l;
+  size_t off = 0;
+  l.q = off;
+  off = align256(off + static_cast<size_t>(B) * h * Lq * d * 2);
+  l.k = off;
+  off = align256(off + static_cast<size_t>(B) * h_kv * Lk * d * 2);
+  l.v = off;
+  off = align256(off + static_cast<size_t>(B) * h_kv * Lk * d * 2);
+  l.o = off;
+  off = align256(off + static_cast<size_t>(B) * h * Lq * d * 2);
+  l.lse = off;
+  off = align256(off + static_cast<size_t>(B) * h * Lq * 4);
+  l.kv = off;
+  off = align256(off + static_cast<size_t>(B) * 4);
+  l.total = off;
+  return l;
+}
+
+attn_status_t host_streams(DeviceState* ds) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (ds->host_in != nullptr) return ATTN_OK;
+  cudaStream_t st[3] = {nullptr, nullptr, nullptr};
+  for (auto& x : st)
+    if (cudaStreamCreateWithFlags(&x, cudaStreamNonBlocking) != cudaSuccess) return ATTN_ERR_CUDA;
+  for (auto& e : ds->host_ev)
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return ATTN_ERR_CUDA;
+  ds->host_out = st[1];
+  ds->host_comp = st[2];
+  ds->host_in = st[0];  // last: marks the set as ready
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd_gqa(const void* Q, const void* K, const void* V, int B, int h, int h_kv,
+                           int Lq, int Lk, int d_k, int d_v, int mask_kind,
+                           const int32_t* kv_lens, float scale, void* O, float* LSE,
+                           void* stream) {
+  // ---- host-side validation (no CUDA call before this point) ----
+  attn_status_t st = check_attn_shape(B, h, h_kv, Lq, Lk, d_k, d_v, mask_kind, scale);
+  if (st != ATTN_OK) return st;
   if (B == 0 || h == 0 || Lq == 0) return ATTN_OK;
   if (!O) return ATTN_ERR_INVALID_ARG;
   if ((mask_kind & ATTN_MASK_PADDING) && !kv_lens) return ATTN_ERR_INVALID_ARG;
@@ -344,21 +423,129 @@ attn_status_t attn_fwd_gqa(const void* Q, const void* K, const void* V, int B, i
     return ATTN_ERR_MISALIGNED;
 
   DeviceState* ds = nullptr;
-  attn_status_t st = device_state(&ds, nullptr);
+  st = device_state(&ds, nullptr);
   if (st != ATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const long long osl = d_v, osh = static_cast<long long>(Lq) * d_v, osb = osh * h;
   if (Lk == 0) {
+    const long long osl = d_v, osh = static_cast<long long>(Lq) * d_v, osb = osh * h;
     gb300::attn_empty_keys_kernel<<<256, 256, 0, s>>>(static_cast<__nv_bfloat16*>(O), osb, osh,
                                                      osl, LSE, B, h, Lq, d_v);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
-  CUtensorMap mq, mk, mv;
-  if ((st = map_bhld(&mq, Q, B, h, Lq, d_k)) != ATTN_OK) return st;
-  if ((st = map_bhld(&mk, K, B, h_kv, Lk, d_k)) != ATTN_OK) return st;
-  if ((st = map_bhld(&mv, V, B, h_kv, Lk, d_v)) != ATTN_OK) return st;
-  return run_attention(ds, mq, mk, mv, 0, B, h, h_kv, Lq, Lk, d_k, mask_kind, kv_lens, scale, O,
-                       osb, osh, osl, LSE, s);
+  return attn_device(ds, Q, K, V, B, h, h_kv, Lq, Lk, d_k, mask_kind, kv_lens, scale, O, LSE, s);
+}
+
+size_t attn_fwd_host_workspace_bytes(int B, int h, int h_kv, int Lq, int Lk, int d_k, int d_v) {
+  if (check_attn_shape(B, h, h_kv, Lq, Lk, d_k, d_v, 0, 0.f) != ATTN_OK) return 0;
+  return host_layout(B, h, h_kv, Lq, Lk, d_k).total;
+}
+
+attn_status_t attn_fwd_host(const void* Q, const void* K, const void* V, int B, int h, int h_kv,
+                            int Lq, int Lk, int d_k, int d_v, int mask_kind,
+                            const int32_t* kv_lens, float scale, void* O, float* LSE,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  attn_status_t st = check_attn_shape(B, h, h_kv, Lq, Lk, d_k, d_v, mask_kind, scale);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || h == 0 || Lq == 0) return ATTN_OK;
+  if (!O || (Lk > 0 && (!Q || !K || !V))) return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ATTN_MASK_PADDING) && !kv_lens) return ATTN_ERR_INVALID_ARG;
+  const HostLayout lay = host_layout(B, h, h_kv, Lq, Lk, d_k);
+  if (!workspace || workspace_bytes < lay.total) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return ATTN_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds, nullptr)) != ATTN_OK) return st;
+  if ((st = host_streams(ds)) != ATTN_OK) return st;
+  std::lock_guard<std::mutex> host_lock(g_host_mutex);
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  __nv_bfloat16* dQ = reinterpret_cast<__nv_bfloat16*>(ws + lay.q);
+  __nv_bfloat16* dK = reinterpret_cast<__nv_bfloat16*>(ws + lay.k);
+  __nv_bfloat16* dV = reinterpret_cast<__nv_bfloat16*>(ws + lay.v);
+  __nv_bfloat16* dO = reinterpret_cast<__nv_bfloat16*>(ws + lay.o);
+  float* dL = LSE ? reinterpret_cast<float*>(ws + lay.lse) : nullptr;
+  int32_t* dkv = (mask_kind & ATTN_MASK_PADDING) ? reinterpret_cast<int32_t*>(ws + lay.kv) : nullptr;
+  const int d = d_k;
+  const int grp = h / h_kv;
+
+  // Chunks of (b, K/V head) units, each with its query heads: whole batch
+  // elements, or a group of K/V heads of one element.  Either way the
+  // chunk's Q, K, V, O and LSE are contiguous, and every chunk has the same
+  // work.  About kHostMaxChunks chunks, of at least 8 MB each.
+  const size_t unit_bytes = static_cast<size_t>(grp) * Lq * d * 2 * 2 +
+                            static_cast<size_t>(Lk) * d * 2 * 2;
+  const size_t total_bytes = unit_bytes * B * h_kv;
+  size_t target = total_bytes / (8u << 20);
+  target = target < 1 ? 1 : (target > static_cast<size_t>(kHostMaxChunks) ? kHostMaxChunks : target);
+  int per_b = 1, per_k = h_kv;  // batch elements / K/V heads per chunk
+  if (target <= static_cast<size_t>(B)) {
+    per_b = static_cast<int>((B + target - 1) / target);
+  } else {
+    const int groups = static_cast<int>((target + B - 1) / B);
+    per_k = (h_kv + groups - 1) / groups;
+  }
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaEvent_t* ev = ds->host_ev;  // [0] start, [1] end, [2 + c % 16] inputs of chunk c, [18 + c % 16] chunk c done
+  cudaError_t e = cudaEventRecord(ev[0], s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->host_in, ev[0], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->host_out, ev[0], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->host_comp, ev[0], 0);
+  if (e == cudaSuccess && dkv)
+    e = cudaMemcpyAsync(dkv, kv_lens, static_cast<size_t>(B) * 4, cudaMemcpyHostToDevice,
+                        ds->host_in);
+  int c = 0;
+  for (int b0 = 0; b0 < B && e == cudaSuccess && st == ATTN_OK; b0 += per_b) {
+    const int nb = (b0 + per_b <= B) ? per_b : B - b0;
+    for (int k0 = 0; k0 < h_kv && e == cudaSuccess && st == ATTN_OK; k0 += per_k, ++c) {
+      const int nk = (k0 + per_k <= h_kv) ? per_k : h_kv - k0;
+      const int hq = nk * grp;  // query heads of each batch element of the chunk
+      const size_t q_off = (static_cast<size_t>(b0) * h + static_cast<size_t>(k0) * grp) * Lq;
+      const size_t kv_off = (static_cast<size_t>(b0) * h_kv + k0) * static_cast<size_t>(Lk);
+      const size_t q_rows = static_cast<size_t>(nb) * hq * Lq;
+      const size_t kv_rows = static_cast<size_t>(nb) * nk * Lk;
+      const size_t rb = static_cast<size_t>(d) * 2;
+      // inputs
+      e = cudaMemcpyAsync(dQ + q_off * d, static_cast<const uint8_t*>(Q) + q_off * rb, q_rows * rb,
+                          cudaMemcpyHostToDevice, ds->host_in);
+      if (e == cudaSuccess && kv_rows > 0)
+        e = cudaMemcpyAsync(dK + kv_off * d, static_cast<const uint8_t*>(K) + kv_off * rb,
+                            kv_rows * rb, cudaMemcpyHostToDevice, ds->host_in);
+      if (e == cudaSuccess && kv_rows > 0)
+        e = cudaMemcpyAsync(dV + kv_off * d, static_cast<const uint8_t*>(V) + kv_off * rb,
+                            kv_rows * rb, cudaMemcpyHostToDevice, ds->host_in);
+      if (e == cudaSuccess) e = cudaEventRecord(ev[2 + c % 16], ds->host_in);
+      // compute: chunks alternate between two streams, so one chunk's last
+      // CTAs and the next chunk's first ones share the GPU
+      cudaStream_t cs = (c & 1) ? ds->host_comp : s;
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[2 + c % 16], 0);
+      if (e != cudaSuccess) break;
+      float* lse_c = dL ? dL + q_off : nullptr;
+      if (Lk == 0) {
+        const long long osl = d, osh = static_cast<long long>(Lq) * d, osb = osh * hq;
+        gb300::attn_empty_keys_kernel<<<256, 256, 0, cs>>>(dO + q_off * d, osb, osh, osl, lse_c,
+                                                            nb, hq, Lq, d);
+        e = cudaGetLastError();
+      } else {
+        st = attn_device(ds, dQ + q_off * d, dK + kv_off * d, dV + kv_off * d, nb, hq, nk, Lq, Lk,
+                         d, mask_kind, dkv ? dkv + b0 : nullptr, scale, dO + q_off * d, lse_c,
+                         cs);
+      }
+      if (e == cudaSuccess && st == ATTN_OK) e = cudaEventRecord(ev[18 + c % 16], cs);
+      // outputs
+      if (e == cudaSuccess && st == ATTN_OK) e = cudaStreamWaitEvent(ds->host_out, ev[18 + c % 16], 0);
+      if (e == cudaSuccess && st == ATTN_OK)
+        e = cudaMemcpyAsync(static_cast<uint8_t*>(O) + q_off * rb, dO + q_off * d, q_rows * rb,
+                            cudaMemcpyDeviceToHost, ds->host_out);
+      if (e == cudaSuccess && st == ATTN_OK && LSE)
+        e = cudaMemcpyAsync(LSE + q_off, lse_c, q_rows * 4, cudaMemcpyDeviceToHost, ds->host_out);
+    }
+  }
+  // the caller's stream completes with the last copy out (which follows
+  // every chunk's kernel)
+  cudaError_t e2 = cudaEventRecord(ev[1], ds->host_out);
+  if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(s, ev[1], 0);
+  if (st != ATTN_OK) return st;
+  return (e == cudaSuccess && e2 == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // extern "C"
