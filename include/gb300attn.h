@@ -237,6 +237,38 @@ attn_status_t mha_layer_fwd(const void* X, const void* W_QKV, const void* W_O, i
                             void* stream);
 
 /*
+ * mha_layer_fwd_host -- mha_layer_fwd with the activations X and Y (and
+ * kv_lens) in HOST memory and the weights W_QKV, W_O on the device, as a
+ * model's parameters are.  The call copies X to the device, runs the layer
+ * and copies Y back, overlapping the three over chunks of whole batch
+ * elements of at least 4096 tokens (at most 8 chunks): a chunk's X is copied
+ * in while the previous chunk computes, and its Y is copied out as soon as it
+ * is done.  Each chunk runs the kernels of mha_layer_fwd on its batch
+ * elements, so with the same attention schedule Y is bit-identical to
+ * mha_layer_fwd's.
+ *
+ *   X, Y, kv_lens   host pointers (page-locked memory lets the copies overlap)
+ *   W_QKV, W_O      device pointers, 16-byte aligned
+ *   workspace       device scratch of at least mha_layer_host_workspace_bytes()
+ *                   bytes, 256-byte aligned: device copies of X, Y, kv_lens and
+ *                   two layer scratch buffers.  Calls that share it must not
+ *                   overlap.
+ *   stream          as for attn_fwd_host: the work runs on internal streams
+ *                   after the work queued on `stream`, and `stream` waits for
+ *                   all of it; Y must not be read before `stream` is
+ *                   synchronised.
+ * Supported shapes and errors as for mha_layer_fwd.
+ */
+attn_status_t mha_layer_fwd_host(const void* X, const void* W_QKV, const void* W_O, int B, int L,
+                                 int d_model, int h, int mask_kind, const int32_t* kv_lens,
+                                 float scale, void* Y, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/* mha_layer_host_workspace_bytes -- workspace of mha_layer_fwd_host; 0 for an
+ * unsupported shape. */
+size_t mha_layer_host_workspace_bytes(int B, int L, int d_model, int h);
+
+/*
  * mha_layer_fwd_noalloc -- the same five-step layer as mha_layer_fwd, for
  * callers that may not allocate device memory: for example a plugin inside a
  * host framework that owns every device buffer through its own pool and does

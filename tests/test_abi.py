@@ -191,3 +191,32 @@ def test_host_entry_validation(cdll):
     # padding mask without kv_lens
     assert f(p, p, p, B, h, hkv, Lq, Lk, d, d, 2, None, 0.0, p, None, ctypes.c_void_p(1 << 20),
              want, None) == 1
+
+
+def test_layer_host_entry_validation(cdll):
+    f = cdll.mha_layer_fwd_host
+    f.restype = ctypes.c_int
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [vp, vp, vp] + [i32] * 5 + [vp, ctypes.c_float, vp, vp, ctypes.c_size_t, vp]
+    ws = cdll.mha_layer_host_workspace_bytes
+    ws.restype = ctypes.c_size_t
+    ws.argtypes = [i32] * 4
+    one = cdll.mha_layer_workspace_bytes
+    one.restype = ctypes.c_size_t
+    one.argtypes = [i32] * 4
+    B, L, dm, h = 8, 2048, 1024, 16
+    def r256(x):
+        return (x + 255) // 256 * 256
+    # chunks of 2 batch elements (4096 tokens): device X and Y, kv_lens and
+    # two layer scratch buffers of one chunk each
+    want = 2 * r256(B * L * dm * 2) + r256(B * 4) + 2 * r256(one(2, L, dm, h))
+    assert ws(B, L, dm, h) == want
+    assert ws(B, L, dm, 5) == 0                      # d_model not a multiple of h
+    host = (ctypes.c_uint8 * 64)()
+    p = ctypes.cast(host, vp)
+    dev = ctypes.c_void_p(1 << 20)
+    assert f(p, dev, dev, B, L, dm, h, 1, None, 0.0, p, None, want, None) == 1      # no workspace
+    assert f(p, dev, dev, B, L, dm, h, 1, None, 0.0, p, dev, want - 256, None) == 1  # too small
+    assert f(p, dev, dev, B, L, dm, h, 1, None, 0.0, p, ctypes.c_void_p((1 << 20) + 16), want,
+             None) == 3                                                                # misaligned
+    assert f(p, dev, dev, B, 100, dm, h, 1, None, 0.0, p, dev, want, None) == 2        # B*L % 128

@@ -99,3 +99,41 @@ def test_host_entry_without_lse_and_without_keys(cuda_lib):
     torch.cuda.current_stream().synchronize()
     g.check_device_status()
     assert torch.all(O0.float() == 0) and torch.all(torch.isneginf(L0))
+
+
+LAYER_CASES = [
+    # (B, L, d_model, h, mask, kv_lens): several chunks of batch elements
+    # (at least 4096 tokens each), and single-chunk shapes
+    (4, 2048, 512, 8, MASK_CAUSAL, None),
+    (6, 1536, 1024, 16, MASK_CAUSAL | MASK_PADDING, [1536, 1000, 1, 0, 777, 1535]),
+    (2, 192, 256, 4, MASK_NONE, None),
+]
+
+
+@pytest.mark.parametrize("case", LAYER_CASES, ids=["x".join(map(str, c[:4])) + "-m%d" % c[4]
+                                                   for c in LAYER_CASES])
+def test_layer_host_entry_equals_device_entry(cuda_lib, schedule, case):
+    """mha_layer_fwd_host runs mha_layer_fwd's kernels on each chunk of batch
+    elements: with the two-Q-tile attention schedule Y is bit-identical; with
+    split keys (whose tile dealing follows each CTA's history) a few
+    attention rows may be summed in the other order, which can move Y by a
+    rounding step."""
+    import torch
+    from sdpa_workloads import make_layer_inputs
+    g = cuda_lib
+    B, L, dm, h, mask, kv = case
+    inp = make_layer_inputs(B, L, dm, seed=B * L + h, w_std=dm ** -0.5)
+    w_qkv, w_o = _host(inp["w_qkv"], pin=False).cuda(), _host(inp["w_o"], pin=False).cuda()
+    kv_host = torch.tensor(kv, dtype=torch.int32) if kv is not None else None
+    Yh = g.mha_layer_fwd_host(_host(inp["x"]), w_qkv, w_o, h, mask_kind=mask, kv_lens=kv_host)
+    torch.cuda.current_stream().synchronize()
+    g.check_device_status()
+    Yd = g.mha_layer_fwd(_host(inp["x"], pin=False).cuda(), w_qkv, w_o, h, mask_kind=mask,
+                         kv_lens=kv_host.cuda() if kv_host is not None else None)
+    g.check_device_status()
+    Yd = Yd.cpu()
+    if schedule == 1:
+        assert torch.equal(Yh.view(torch.int16), Yd.view(torch.int16))
+    else:
+        err = (Yh.float() - Yd.float()).abs()
+        assert torch.all(err <= 2.0 ** -7 * Yd.float().abs() + 1e-3), err.max().item()

@@ -21,7 +21,8 @@ __all__ = [
     "MASK_NONE", "MASK_CAUSAL", "MASK_PADDING", "MASK_CAUSAL_BOTTOM_RIGHT", "AttnError", "attn_fwd",
     "attn_fwd_host", "attn_fwd_host_workspace_bytes", "attn_decode", "attn_decode_workspace_bytes",
     "attn_weights", "mha_layer_fwd",
-    "mha_layer_workspace_bytes", "mha_layer_fwd_noalloc", "NOALLOC_SCRATCH_BYTES", "gemm_bf16",
+    "mha_layer_workspace_bytes", "mha_layer_fwd_noalloc", "mha_layer_fwd_host",
+    "mha_layer_host_workspace_bytes", "NOALLOC_SCRATCH_BYTES", "gemm_bf16",
     "check_device_status", "set_wait_limit_ns", "set_schedule", "SCHEDULE_AUTO",
     "SCHEDULE_TWO_QTILES", "SCHEDULE_SPLIT_KEYS", "debug_skip_kv_load", "probe_ex2", "PROBE_EX2_PER_THREAD_ITER", "library_path", "lib",
 ]
@@ -84,6 +85,10 @@ def _load():
     L.mha_layer_workspace_bytes.argtypes = [i32, i32, i32, i32]
     L.mha_layer_fwd.restype = i32
     L.mha_layer_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, f32, vp, vp, sz, vp]
+    L.mha_layer_fwd_host.restype = i32
+    L.mha_layer_fwd_host.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, f32, vp, vp, sz, vp]
+    L.mha_layer_host_workspace_bytes.restype = sz
+    L.mha_layer_host_workspace_bytes.argtypes = [i32, i32, i32, i32]
     L.mha_layer_fwd_noalloc.restype = i32
     L.mha_layer_fwd_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, f32, vp, vp]
     L.attn_gemm_bf16.restype = i32
@@ -379,3 +384,36 @@ def probe_ex2(blocks, threads, iters, timing, sink, stream=None):
     _dev_tensor(sink, "sink", torch.float32)
     _check(lib.attn_probe_ex2(int(blocks), int(threads), int(iters), _ptr(timing), _ptr(sink),
                               _stream_handle(stream)), "attn_probe_ex2")
+
+
+def mha_layer_host_workspace_bytes(B, L, d_model, h):
+    return int(lib.mha_layer_host_workspace_bytes(int(B), int(L), int(d_model), int(h)))
+
+
+def mha_layer_fwd_host(x, w_qkv, w_o, num_heads, mask_kind=MASK_NONE, kv_lens=None, scale=None,
+                       out=None, workspace=None, stream=None):
+    """The five-step layer on a host (CPU) activation x [B, L, d_model] with
+    device weights; Y comes back into a host tensor.  The copies overlap the
+    kernels over chunks of batch elements.  ``kv_lens`` is an int32 CPU tensor.
+    The result is valid once ``stream`` has been synchronised."""
+    _host_tensor(x, "x", torch.bfloat16)
+    _dev_tensor(w_qkv, "w_qkv", torch.bfloat16)
+    _dev_tensor(w_o, "w_o", torch.bfloat16)
+    B, L, dm = x.shape
+    if tuple(w_qkv.shape) != (dm, 3 * dm) or tuple(w_o.shape) != (dm, dm):
+        raise ValueError("weight shapes do not match d_model")
+    if out is None:
+        out = torch.empty((B, L, dm), dtype=torch.bfloat16).pin_memory()
+    _host_tensor(out, "out", torch.bfloat16)
+    if kv_lens is not None:
+        _host_tensor(kv_lens, "kv_lens", torch.int32)
+    need = mha_layer_host_workspace_bytes(B, L, dm, num_heads)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=w_qkv.device)
+    _dev_tensor(workspace, "workspace", torch.uint8)
+    st = lib.mha_layer_fwd_host(_ptr(x), _ptr(w_qkv), _ptr(w_o), B, L, dm, int(num_heads),
+                                int(mask_kind),
+                                _ptr(kv_lens), float(scale) if scale else 0.0, _ptr(out),
+                                _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(st, "mha_layer_fwd_host")
+    return out

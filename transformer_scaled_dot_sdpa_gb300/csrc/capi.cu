@@ -388,6 +388,71 @@ HostLayout host_layout(int B, int h, int h_kv, int Lq, int Lk, int d) {
   return l;
 }
 
+// The five-step layer on device buffers (arguments already validated).
+attn_status_t layer_device(DeviceState* ds, const void* X, const void* W_QKV, const void* W_O,
+                           int B, int L, int d_model, int h, int mask_kind,
+                           const int32_t* kv_lens, float scale, void* Y, uint8_t* ws,
+                           cudaStream_t s) {
+  const int dk = d_model / h;
+  const long long rows = static_cast<long long>(B) * L;
+  const size_t qkv_bytes = static_cast<size_t>(rows) * 3 * d_model * 2;
+  uint8_t* qkv = ws;
+  uint8_t* cat = ws + ((qkv_bytes + 255) & ~static_cast<size_t>(255));
+  attn_status_t st;
+  // step 1: QKV = X W_QKV  -> [B, L, 3, h, d_k]
+  if ((st = run_gemm(ds, X, W_QKV, qkv, static_cast<int>(rows), 3 * d_model, d_model, s)) !=
+      ATTN_OK)
+    return st;
+  // steps 2-4: split heads (strided tensor maps), attention, concat (strided store)
+  CUtensorMap mq, mk, mv;
+  const size_t blk = static_cast<size_t>(d_model) * 2;
+  if ((st = map_packed(&mq, qkv, B, h, L, dk)) != ATTN_OK) return st;
+  if ((st = map_packed(&mk, qkv + blk, B, h, L, dk)) != ATTN_OK) return st;
+  if ((st = map_packed(&mv, qkv + 2 * blk, B, h, L, dk)) != ATTN_OK) return st;
+  if ((st = run_attention(ds, mq, mk, mv, 1, B, h, h, L, L, dk, mask_kind, kv_lens, scale, cat,
+                          static_cast<long long>(L) * d_model, dk, d_model, nullptr, s)) !=
+      ATTN_OK)
+    return st;
+  // step 5: Y = Concat W_O
+  return run_gemm(ds, cat, W_O, Y, static_cast<int>(rows), d_model, d_model, s);
+}
+
+// mha_layer_fwd_host: chunks of whole batch elements of at least 4096 tokens
+// (so the projection GEMMs keep several waves of 256 x 256 tiles), at most 8;
+// the workspace holds the device copies of X and Y, kv_lens and one layer
+// scratch per compute stream.
+struct LayerHostPlan {
+  int per_b;
+  size_t x, y, kv, scratch[2], total;
+};
+
+LayerHostPlan layer_host_plan(int B, int L, int d_model, int h) {
+  LayerHostPlan pl;
+  const long long rows = static_cast<long long>(B) * L;
+  long long chunks = rows / 4096;
+  chunks = chunks < 1 ? 1 : (chunks > 8 ? 8 : chunks);
+  int per_b = static_cast<int>((B + chunks - 1) / chunks);
+  // every chunk's rows must stay a multiple of the GEMM's 128-row tiles
+  while (per_b < B && (static_cast<long long>(per_b) * L) % gb300::GEMM_BM_CTA != 0) ++per_b;
+  if ((static_cast<long long>(per_b) * L) % gb300::GEMM_BM_CTA != 0) per_b = B;
+  pl.per_b = per_b;
+  const size_t xy = static_cast<size_t>(rows) * d_model * 2;
+  const size_t scratch = mha_layer_workspace_bytes(per_b, L, d_model, h);
+  size_t off = 0;
+  pl.x = off;
+  off = align256(off + xy);
+  pl.y = off;
+  off = align256(off + xy);
+  pl.kv = off;
+  off = align256(off + static_cast<size_t>(B) * 4);
+  pl.scratch[0] = off;
+  off = align256(off + scratch);
+  pl.scratch[1] = off;
+  off = align256(off + scratch);
+  pl.total = off;
+  return pl;
+}
+
 attn_status_t host_streams(DeviceState* ds) {
   std::lock_guard<std::mutex> lock(g_mutex);
   if (ds->host_in != nullptr) return ATTN_OK;
@@ -774,27 +839,85 @@ attn_status_t mha_layer_fwd(const void* X, const void* W_QKV, const void* W_O, i
   DeviceState* ds = nullptr;
   attn_status_t st = device_state(&ds, nullptr);
   if (st != ATTN_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return layer_device(ds, X, W_QKV, W_O, B, L, d_model, h, mask_kind, kv_lens, scale, Y,
+                      static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+size_t mha_layer_host_workspace_bytes(int B, int L, int d_model, int h) {
+  const size_t one = mha_layer_workspace_bytes(B, L, d_model, h);
+  if (one == 0) return 0;
+  const LayerHostPlan pl = layer_host_plan(B, L, d_model, h);
+  return pl.total;
+}
+
+attn_status_t mha_layer_fwd_host(const void* X, const void* W_QKV, const void* W_O, int B, int L,
+                                 int d_model, int h, int mask_kind, const int32_t* kv_lens,
+                                 float scale, void* Y, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  if (B < 0 || L < 0 || d_model <= 0 || h <= 0) return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_PADDING | ATTN_MASK_CAUSAL_BOTTOM_RIGHT)) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ATTN_MASK_CAUSAL) && (mask_kind & ATTN_MASK_CAUSAL_BOTTOM_RIGHT))
+    return ATTN_ERR_INVALID_ARG;
+  if (!(scale == scale) || std::isinf(scale)) return ATTN_ERR_INVALID_ARG;
+  if (d_model % h != 0) return ATTN_ERR_INVALID_ARG;
+  const int dk = d_model / h;
+  if (dk != 64 && dk != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d_model % gb300::GEMM_BN != 0) return ATTN_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(B) * L;
+  if (rows % gb300::GEMM_BM_CTA != 0 || rows >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  if (rows == 0) return ATTN_OK;
+  if (!X || !W_QKV || !W_O || !Y || !workspace) return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ATTN_MASK_PADDING) && !kv_lens) return ATTN_ERR_INVALID_ARG;
+  const LayerHostPlan pl = layer_host_plan(B, L, d_model, h);
+  if (workspace_bytes < pl.total) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(W_QKV, 16) || !aligned(W_O, 16) || !aligned(workspace, 256))
+    return ATTN_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  attn_status_t st = device_state(&ds, nullptr);
+  if (st != ATTN_OK) return st;
+  if ((st = host_streams(ds)) != ATTN_OK) return st;
+  std::lock_guard<std::mutex> host_lock(g_host_mutex);
+
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const size_t qkv_bytes = static_cast<size_t>(rows) * 3 * d_model * 2;
-  uint8_t* qkv = ws;
-  uint8_t* cat = ws + ((qkv_bytes + 255) & ~static_cast<size_t>(255));
-  // step 1: QKV = X W_QKV  -> [B, L, 3, h, d_k]
-  if ((st = run_gemm(ds, X, W_QKV, qkv, static_cast<int>(rows), 3 * d_model, d_model, s)) !=
-      ATTN_OK)
-    return st;
-  // steps 2-4: split heads (strided tensor maps), attention, concat (strided store)
-  CUtensorMap mq, mk, mv;
-  const size_t blk = static_cast<size_t>(d_model) * 2;
-  if ((st = map_packed(&mq, qkv, B, h, L, dk)) != ATTN_OK) return st;
-  if ((st = map_packed(&mk, qkv + blk, B, h, L, dk)) != ATTN_OK) return st;
-  if ((st = map_packed(&mv, qkv + 2 * blk, B, h, L, dk)) != ATTN_OK) return st;
-  if ((st = run_attention(ds, mq, mk, mv, 1, B, h, h, L, L, dk, mask_kind, kv_lens, scale, cat,
-                          static_cast<long long>(L) * d_model, dk, d_model, nullptr, s)) !=
-      ATTN_OK)
-    return st;
-  // step 5: Y = Concat W_O
-  return run_gemm(ds, cat, W_O, Y, static_cast<int>(rows), d_model, d_model, s);
+  uint8_t* dX = ws + pl.x;
+  uint8_t* dY = ws + pl.y;
+  int32_t* dkv = (mask_kind & ATTN_MASK_PADDING) ? reinterpret_cast<int32_t*>(ws + pl.kv) : nullptr;
+  const size_t row_bytes = static_cast<size_t>(d_model) * 2;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaEvent_t* ev = ds->host_ev;  // as in attn_fwd_host
+  cudaError_t e = cudaEventRecord(ev[0], s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->host_in, ev[0], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->host_out, ev[0], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->host_comp, ev[0], 0);
+  if (e == cudaSuccess && dkv)
+    e = cudaMemcpyAsync(dkv, kv_lens, static_cast<size_t>(B) * 4, cudaMemcpyHostToDevice,
+                        ds->host_in);
+  int c = 0;
+  for (int b0 = 0; b0 < B && e == cudaSuccess && st == ATTN_OK; b0 += pl.per_b, ++c) {
+    const int nb = (b0 + pl.per_b <= B) ? pl.per_b : B - b0;
+    const size_t off = static_cast<size_t>(b0) * L * row_bytes;
+    const size_t bytes = static_cast<size_t>(nb) * L * row_bytes;
+    e = cudaMemcpyAsync(dX + off, static_cast<const uint8_t*>(X) + off, bytes,
+                        cudaMemcpyHostToDevice, ds->host_in);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[2 + c % 16], ds->host_in);
+    // the two compute streams alternate, each with its own layer scratch
+    cudaStream_t cs = (c & 1) ? ds->host_comp : s;
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[2 + c % 16], 0);
+    if (e != cudaSuccess) break;
+    st = layer_device(ds, dX + off, W_QKV, W_O, nb, L, d_model, h, mask_kind,
+                      dkv ? dkv + b0 : nullptr, scale, dY + off, ws + pl.scratch[c & 1], cs);
+    if (st != ATTN_OK) break;
+    e = cudaEventRecord(ev[18 + c % 16], cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->host_out, ev[18 + c % 16], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<uint8_t*>(Y) + off, dY + off, bytes, cudaMemcpyDeviceToHost,
+                          ds->host_out);
+  }
+  cudaError_t e2 = cudaEventRecord(ev[1], ds->host_out);
+  if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(s, ev[1], 0);
+  if (st != ATTN_OK) return st;
+  return (e == cudaSuccess && e2 == cudaSuccess) ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status_t mha_layer_fwd_noalloc(const void* X, const void* W_QKV, const void* W_O, int B,
