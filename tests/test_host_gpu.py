@@ -13,7 +13,7 @@ import oracle
 from sdpa_workloads import MASK_CAUSAL, MASK_NONE, MASK_PADDING, make_attention_inputs
 from tests.parity_util import compare_attention
 
-pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("schedule")]
+pytestmark = pytest.mark.gpu
 
 BR = 4  # causal, aligned to the last key
 
@@ -137,3 +137,38 @@ def test_layer_host_entry_equals_device_entry(cuda_lib, schedule, case):
     else:
         err = (Yh.float() - Yd.float()).abs()
         assert torch.all(err <= 2.0 ** -7 * Yd.float().abs() + 1e-3), err.max().item()
+
+
+def test_host_entries_at_full_size(cuda_lib):
+    """The launch configurations the benchmark's end-to-end figures time: the
+    long-context causal workload through attn_fwd_host and the layer workload
+    through mha_layer_fwd_host, each bit-identical to the device-buffer call
+    (two-Q-tile schedule), whose rows the sampled full-size parity tests
+    check against the oracle."""
+    import torch
+    from sdpa_workloads import make_workload_inputs
+    g = cuda_lib
+    g.set_schedule(1)
+    try:
+        inp = make_workload_inputs("mha_causal_longctx_b1_h32_l32768_d128")
+        Oh, Lh = g.attn_fwd_host(_host(inp["q"]), _host(inp["k"]), _host(inp["v"]),
+                                 mask_kind=MASK_CAUSAL)
+        torch.cuda.current_stream().synchronize()
+        g.check_device_status()
+        dev = lambda b: _host(b, pin=False).cuda()
+        Od, Ld = g.attn_fwd(dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), mask_kind=MASK_CAUSAL)
+        g.check_device_status()
+        assert torch.equal(Oh.view(torch.int16), Od.cpu().view(torch.int16))
+        assert torch.equal(Lh.view(torch.int32), Ld.cpu().view(torch.int32))
+        del Od, Ld, Oh, Lh, inp
+
+        lay = make_workload_inputs("mha_layer_causal_b8_l2048_dm1024_h16")
+        w_qkv, w_o = dev(lay["w_qkv"]), dev(lay["w_o"])
+        Yh = g.mha_layer_fwd_host(_host(lay["x"]), w_qkv, w_o, 16, mask_kind=MASK_CAUSAL)
+        torch.cuda.current_stream().synchronize()
+        g.check_device_status()
+        Yd = g.mha_layer_fwd(dev(lay["x"]), w_qkv, w_o, 16, mask_kind=MASK_CAUSAL)
+        g.check_device_status()
+        assert torch.equal(Yh.view(torch.int16), Yd.cpu().view(torch.int16))
+    finally:
+        g.set_schedule(0)
