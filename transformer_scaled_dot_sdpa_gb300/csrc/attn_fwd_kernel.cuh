@@ -77,7 +77,7 @@ struct AttnParams {
   __nv_bfloat16* O;
   long long o_stride_b, o_stride_h, o_stride_l;  // in elements
   float* LSE;              // [B,H,Lq] natural-log LSE, or nullptr
-  int n_qblocks;           // ceil(Lq / 256) (ceil(Lq / 128) in the split kernel)
+  int n_qblocks;           // ceil(Lq / 256)
   int n_items;             // B * H * n_qblocks
   unsigned int* status;    // device status word
   unsigned long long wait_limit_ns;
