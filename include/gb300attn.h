@@ -48,8 +48,12 @@ typedef enum {
   ATTN_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned            */
   ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed            */
   ATTN_ERR_TIMEOUT = 5,      /* a device-side pipeline wait gave up          */
-  ATTN_ERR_TOO_LARGE = 6     /* problem exceeds the fixed scratch of
+  ATTN_ERR_TOO_LARGE = 6,    /* problem exceeds the fixed scratch of
                                 mha_layer_fwd_noalloc                       */
+  ATTN_ERR_SELF_CHECK = 7    /* the self-checking build found a TMA or TMEM
+                                access that broke its rules (skipped, not
+                                executed); never returned by the normal
+                                build                                       */
 } attn_status_t;
 
 /*
@@ -320,6 +324,19 @@ attn_status_t attn_gemm_bf16(const void* A, const void* B, void* C, int M, int N
  * CUDA error, else ATTN_OK.
  */
 attn_status_t attn_check_device_status(void* stream);
+
+/*
+ * attn_is_checked_build -- 1 for the self-checking build of this library
+ * (libgb300attn_checked.so), 0 otherwise.  The self-checking build tests,
+ * before every TMA copy and TMEM load or store, the preconditions that the
+ * hardware does not check by itself: the innermost TMA coordinate on a
+ * 16-byte boundary (and no store below coordinate 0), tile and barrier
+ * addresses aligned, and each warp's TMEM access inside its 32-lane quarter
+ * and the 512 columns.  A violation skips the access and makes the next
+ * attn_check_device_status return ATTN_ERR_SELF_CHECK.  Results are
+ * otherwise identical to the normal build's.
+ */
+int attn_is_checked_build(void);
 
 /* attn_status_string -- static, human-readable name of a status code. */
 const char* attn_status_string(attn_status_t status);

@@ -24,7 +24,7 @@ __all__ = [
     "mha_layer_workspace_bytes", "mha_layer_fwd_noalloc", "mha_layer_fwd_host",
     "mha_layer_host_workspace_bytes", "NOALLOC_SCRATCH_BYTES", "gemm_bf16",
     "check_device_status", "set_wait_limit_ns", "set_schedule", "SCHEDULE_AUTO",
-    "SCHEDULE_TWO_QTILES", "SCHEDULE_SPLIT_KEYS", "debug_skip_kv_load", "probe_ex2", "PROBE_EX2_PER_THREAD_ITER", "library_path", "lib",
+    "SCHEDULE_TWO_QTILES", "SCHEDULE_SPLIT_KEYS", "debug_skip_kv_load", "is_checked_build", "probe_ex2", "PROBE_EX2_PER_THREAD_ITER", "library_path", "lib",
 ]
 
 MASK_NONE = 0
@@ -40,11 +40,15 @@ SCHEDULE_SPLIT_KEYS = 2
 ATTN_OK = 0
 STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
                 3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_TIMEOUT",
-                6: "ATTN_ERR_TOO_LARGE"}
+                6: "ATTN_ERR_TOO_LARGE", 7: "ATTN_ERR_SELF_CHECK"}
 NOALLOC_SCRATCH_BYTES = 32 << 20  # ATTN_NOALLOC_SCRATCH_BYTES
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-library_path = os.path.join(_HERE, "libgb300attn.so")
+# GB300ATTN_CHECKED=1 in the environment (read at import) selects the
+# self-checking build libgb300attn_checked.so (see attn_is_checked_build)
+_LIB_NAME = ("libgb300attn_checked.so" if os.environ.get("GB300ATTN_CHECKED", "0") == "1"
+             else "libgb300attn.so")
+library_path = os.path.join(_HERE, _LIB_NAME)
 
 
 class AttnError(RuntimeError):
@@ -59,8 +63,9 @@ class AttnError(RuntimeError):
 def _load():
     if not os.path.exists(library_path):
         raise ImportError(
-            "libgb300attn.so is not built (expected at %s); run "
-            "`python transformer_scaled_dot_sdpa_gb300/build.py`" % library_path)
+            "%s is not built (expected at %s); run "
+            "`python transformer_scaled_dot_sdpa_gb300/build.py%s`"
+            % (_LIB_NAME, library_path, " --checked" if "checked" in _LIB_NAME else ""))
     L = ctypes.CDLL(library_path)
     vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float,
                              ctypes.c_size_t)
@@ -93,6 +98,8 @@ def _load():
     L.mha_layer_fwd_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, f32, vp, vp]
     L.attn_gemm_bf16.restype = i32
     L.attn_gemm_bf16.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+    L.attn_is_checked_build.restype = i32
+    L.attn_is_checked_build.argtypes = []
     L.attn_check_device_status.restype = i32
     L.attn_check_device_status.argtypes = [vp]
     L.attn_status_string.restype = ctypes.c_char_p
@@ -417,3 +424,8 @@ def mha_layer_fwd_host(x, w_qkv, w_o, num_heads, mask_kind=MASK_NONE, kv_lens=No
                                 _ptr(workspace), workspace.numel(), _stream_handle(stream))
     _check(st, "mha_layer_fwd_host")
     return out
+
+
+def is_checked_build():
+    """True when the loaded library is the self-checking build."""
+    return bool(lib.attn_is_checked_build())

@@ -281,6 +281,7 @@ const char* attn_status_string(attn_status_t s) {
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
     case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
     case ATTN_ERR_TOO_LARGE: return "ATTN_ERR_TOO_LARGE";
+    case ATTN_ERR_SELF_CHECK: return "ATTN_ERR_SELF_CHECK";
   }
   return "ATTN_STATUS_UNKNOWN";
 }
@@ -958,9 +959,28 @@ attn_status_t attn_check_device_status(void* stream) {
     if (cudaMemcpy(ds->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
       return ATTN_ERR_CUDA;
   }
+#ifdef GB300_CHECKED
+  unsigned int checks = 0;
+  if (cudaMemcpyFromSymbol(&checks, gb300::g_check_word, sizeof checks) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (checks != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(gb300::g_check_word, &zero, sizeof zero) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    return ATTN_ERR_SELF_CHECK;
+  }
+#endif
   if (word & gb300::ATTN_STATUS_TIMEOUT) return ATTN_ERR_TIMEOUT;
   if (word & gb300::ATTN_STATUS_BAD_KVLEN) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
+}
+
+int attn_is_checked_build(void) {
+#ifdef GB300_CHECKED
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 }  // extern "C"

@@ -12,6 +12,45 @@
 
 namespace gb300 {
 
+// ---------------------------------------------------------------------------
+// Self-checks (the checked build, compiled with GB300_CHECKED): the
+// preconditions of the TMA and tcgen05 operations below are tested before
+// each one; a violation sets a bit in g_check_word (read and cleared by
+// attn_check_device_status, which then returns ATTN_ERR_SELF_CHECK) and the
+// operation is skipped, so nothing faults or traps.  The predicates are
+// host/device functions so that they can be tested on the CPU.
+// ---------------------------------------------------------------------------
+enum : unsigned int {
+  CHECK_TMA_COORD = 1u,   // innermost TMA coordinate not on 16 bytes, or a store below 0
+  CHECK_SMEM_ALIGN = 2u,  // TMA tile / mbarrier address not aligned
+  CHECK_TMEM_ADDR = 4u,   // TMEM access outside the warp's lane quarter or past 512 columns
+};
+// innermost coordinate of a tiled TMA copy: a multiple of 16 bytes
+__host__ __device__ constexpr bool tma_inner_coord_ok(int c0, int elem_bytes) {
+  return c0 >= 0 ? (c0 * elem_bytes) % 16 == 0 : ((-c0) * elem_bytes) % 16 == 0;
+}
+// tile of a 128-byte-swizzled tensor map: 1024-byte aligned
+__host__ __device__ constexpr bool swizzled_tile_ok(uint32_t smem_addr) {
+  return (smem_addr & 1023u) == 0u;
+}
+// tcgen05.ld / st of 32 lanes x ncols columns by a warp of the given index
+// within its warpgroup: lane field = 32 x (warp % 4), columns in [0, 512)
+__host__ __device__ constexpr bool tmem_warp_access_ok(uint32_t taddr, uint32_t ncols,
+                                                       uint32_t warp) {
+  return (taddr >> 16) == 32u * (warp & 3u) && (taddr & 0xFFFFu) + ncols <= 512u;
+}
+#ifdef GB300_CHECKED
+__device__ unsigned int g_check_word;
+__device__ __forceinline__ bool check_ok(bool cond, unsigned int bit) {
+  if (!cond) atomicOr(&g_check_word, bit);
+  return cond;
+}
+#define GB300_CHECK(cond, bit) \
+  if (!::gb300::check_ok((cond), (bit))) return
+#else
+#define GB300_CHECK(cond, bit) ((void)0)
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -104,6 +143,8 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int c0, int c1, int c2, int c3) {
+  GB300_CHECK(tma_inner_coord_ok(c0, 2), CHECK_TMA_COORD);
+  GB300_CHECK(swizzled_tile_ok(smem_u32(dst)) && (smem_u32(bar) & 7u) == 0u, CHECK_SMEM_ALIGN);
   asm volatile(
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
@@ -114,6 +155,8 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int c0, int c1) {
+  GB300_CHECK(tma_inner_coord_ok(c0, 2), CHECK_TMA_COORD);
+  GB300_CHECK(swizzled_tile_ok(smem_u32(dst)) && (smem_u32(bar) & 7u) == 0u, CHECK_SMEM_ALIGN);
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
@@ -156,6 +199,8 @@ __device__ __forceinline__ void cluster_sync() {
 // signalled on an mbarrier of either CTA of the pair (shared::cluster address)
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
                                                  uint32_t mbar_cluster, int c0, int c1) {
+  GB300_CHECK(tma_inner_coord_ok(c0, 2), CHECK_TMA_COORD);
+  GB300_CHECK(swizzled_tile_ok(smem_u32(dst)) && (mbar_cluster & 7u) == 0u, CHECK_SMEM_ALIGN);
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".cta_group::2 [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
@@ -167,6 +212,8 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
 // tracked per thread with bulk groups
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0,
                                              int c1) {
+  GB300_CHECK(c0 >= 0 && c1 >= 0 && tma_inner_coord_ok(c0, 2), CHECK_TMA_COORD);
+  GB300_CHECK(swizzled_tile_ok(smem_u32(src)), CHECK_SMEM_ALIGN);
   asm volatile(
       "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
           reinterpret_cast<uint64_t>(map)),
@@ -341,6 +388,12 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 // TMEM <-> registers, 32 lanes x 32 columns of 32 bit per warp.  A warp may
 // only touch the 32-lane quarter selected by (warp index % 4).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+#ifdef GB300_CHECKED
+  if (!check_ok(tmem_warp_access_ok(taddr, 32u, threadIdx.x >> 5), CHECK_TMEM_ADDR)) {
+    for (int i = 0; i < 32; ++i) r[i] = 0u;
+    return;
+  }
+#endif
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,"
@@ -355,6 +408,7 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 }
 
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  GB300_CHECK(tmem_warp_access_ok(taddr, 32u, threadIdx.x >> 5), CHECK_TMEM_ADDR);
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
       "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,"
