@@ -332,7 +332,9 @@ attn_status_t attn_check_device_status(void* stream);
  * hardware does not check by itself: the innermost TMA coordinate on a
  * 16-byte boundary (and no store below coordinate 0), tile and barrier
  * addresses aligned, and each warp's TMEM access inside its 32-lane quarter
- * and the 512 columns.  A violation skips the access and makes the next
+ * and the 512 columns; and it checks that every attention work item decodes
+ * to a batch element, head and row block in range.  A violation skips the
+ * access (an out-of-range item ends the CTA's work) and makes the next
  * attn_check_device_status return ATTN_ERR_SELF_CHECK.  Results are
  * otherwise identical to the normal build's.
  */

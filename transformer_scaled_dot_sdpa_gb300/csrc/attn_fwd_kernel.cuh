@@ -157,6 +157,13 @@ __device__ __forceinline__ bool attn_get_item(const AttnParams& p, int k, AttnIt
   it.b = bh / p.H;
   it.h = bh - it.b * p.H;
   it.kvh = it.h / p.kv_group;
+#ifdef GB300_CHECKED
+  // every role decodes the same k, so all of them stop at the same item
+  if (!check_ok(it.b >= 0 && it.b < p.B && it.h >= 0 && it.h < p.H && qb >= 0 &&
+                    qb < p.n_qblocks && it.kvh < p.H / p.kv_group,
+                CHECK_ITEM))
+    return false;
+#endif
   int kv_len = p.Lk;
   it.kv_len_raw = p.Lk;
   if (p.mask_kind & ATTN_MASK_PADDING_BIT) {

@@ -63,6 +63,12 @@ __device__ __forceinline__ bool split_get_item(const AttnParams& p, int k, Split
     it.b = bk / hkv;
     it.kvh = bk - it.b * hkv;
     it.h = it.kvh * p.kv_group;
+#ifdef GB300_CHECKED
+    if (!check_ok(it.b >= 0 && it.b < p.B && it.kvh >= 0 && it.kvh < hkv && it.chunk >= 0 &&
+                      it.chunk < p.n_chunks,
+                  CHECK_ITEM))
+      return false;
+#endif
     it.qrow = (it.b * p.H + it.h) * p.Lq;
     int kv_len = p.Lk;
     it.kv_len_raw = p.Lk;
@@ -91,6 +97,13 @@ __device__ __forceinline__ bool split_get_item(const AttnParams& p, int k, Split
   it.b = bh / p.H;
   it.h = bh - it.b * p.H;
   it.kvh = it.h / p.kv_group;
+#ifdef GB300_CHECKED
+  // every role decodes the same k, so all of them stop at the same item
+  if (!check_ok(it.b >= 0 && it.b < p.B && it.h >= 0 && it.h < p.H && qt >= 0 &&
+                    qt < p.n_qblocks && it.kvh < p.H / p.kv_group,
+                CHECK_ITEM))
+    return false;
+#endif
   int kv_len = p.Lk;
   it.kv_len_raw = p.Lk;
   if (p.mask_kind & ATTN_MASK_PADDING_BIT) {

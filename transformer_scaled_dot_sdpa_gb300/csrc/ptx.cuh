@@ -24,6 +24,7 @@ enum : unsigned int {
   CHECK_TMA_COORD = 1u,   // innermost TMA coordinate not on 16 bytes, or a store below 0
   CHECK_SMEM_ALIGN = 2u,  // TMA tile / mbarrier address not aligned
   CHECK_TMEM_ADDR = 4u,   // TMEM access outside the warp's lane quarter or past 512 columns
+  CHECK_ITEM = 8u,        // a work item decoded to a batch / head / row block out of range
 };
 // innermost coordinate of a tiled TMA copy: a multiple of 16 bytes
 __host__ __device__ constexpr bool tma_inner_coord_ok(int c0, int elem_bytes) {
