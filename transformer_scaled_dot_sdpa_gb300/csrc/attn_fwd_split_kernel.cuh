@@ -690,38 +690,58 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
 // ---------------------------------------------------------------------------
 // split-KV decode: merge the chunks' partial softmaxes of every query row
 // ---------------------------------------------------------------------------
-// One warp per query row (b, h, q); lane l holds output columns l, l + 32, ...
-// With m = max_c m_c and w_c = 2^(m_c - m):
+// One warp per query row (b, h, q).  With m = max_c m_c and w_c = 2^(m_c - m):
 //   O = sum_c w_c Opart_c / sum_c w_c lb_c,   LSE = (m + log2 sum_c w_c l_c) ln 2,
 // the identity by which the online softmax merges partial results
 // ("Self-Attention 机制", Softmax 的数值稳定性与 Online Softmax).  Rows whose
 // every chunk is empty (padded or without keys) get O = 0 and LSE = -inf.
+// Lane c reads the (m, l, lb) of chunks c, c + 32, ... and the warp reduces
+// them with shuffles, so the statistics cost one round trip to memory, not
+// one per chunk.  Then lane l accumulates output columns l, l + 32, ... over
+// the chunks in chunk order, with several chunks' loads in flight.
 template <int D>
 __global__ void __launch_bounds__(128)
     attn_decode_combine_kernel(const float* __restrict__ part_o,
                                const float* __restrict__ part_ml, int n_chunks, long long rows,
                                __nv_bfloat16* __restrict__ O, float* __restrict__ LSE) {
   constexpr int PER = D / 32;
+  constexpr unsigned FULL = 0xffffffffu;
   const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31u);
-  if (row >= rows) return;
-  const float* ml = part_ml + row * n_chunks * 4;
+  if (row >= rows) return;  // uniform over the warp
+  const float4* ml = reinterpret_cast<const float4*>(part_ml + row * n_chunks * 4);
   float mm = -INFINITY;
-  for (int c = 0; c < n_chunks; ++c) mm = fmaxf(mm, ml[c * 4]);
+  for (int c = lane; c < n_chunks; c += 32) mm = fmaxf(mm, ml[c].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(FULL, mm, o));
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
   float l = 0.f, lb = 0.f;
   if (mm != -INFINITY) {
-    for (int c = 0; c < n_chunks; ++c) {
-      const float mc = ml[c * 4];
-      if (mc == -INFINITY) continue;
-      const float w = ex2_approx(mc - mm);
-      l += w * ml[c * 4 + 1];
-      lb += w * ml[c * 4 + 2];
-      const float* po = part_o + (row * n_chunks + c) * D;
+    for (int c0 = 0; c0 < n_chunks; c0 += 32) {
+      float w = 0.f;  // weight of chunk c0 + lane; 0 for an empty chunk
+      if (c0 + lane < n_chunks) {
+        const float4 v = ml[c0 + lane];
+        if (v.x != -INFINITY) {
+          w = ex2_approx(v.x - mm);
+          l += w * v.y;
+          lb += w * v.z;
+        }
+      }
+      const int nc = min(32, n_chunks - c0);
+      const float* po = part_o + (row * n_chunks + c0) * D + lane;
+#pragma unroll 4
+      for (int j = 0; j < nc; ++j) {
+        const float wj = __shfl_sync(FULL, w, j);
 #pragma unroll
-      for (int i = 0; i < PER; ++i) acc[i] += w * po[lane + 32 * i];
+        for (int i = 0; i < PER; ++i) acc[i] += wj * po[static_cast<long long>(j) * D + 32 * i];
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      l += __shfl_xor_sync(FULL, l, o);
+      lb += __shfl_xor_sync(FULL, lb, o);
     }
   }
   const bool zero = !(lb > 0.f);
