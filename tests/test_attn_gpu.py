@@ -98,6 +98,26 @@ def test_deterministic(cuda_lib):
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_output_aligned_to_16_bytes_only(cuda_lib, d):
+    """O whose base is 16- but not 32-byte aligned (the API's minimum): the
+    kernels then store O rows in 16-byte pieces instead of 32-byte ones, with
+    the same values bit for bit."""
+    import torch
+    g = cuda_lib
+    B, H, L = 2, 3, 700
+    inp = make_attention_inputs(B, H, L, L, d, d, seed=21)
+    q, k, v = up(inp["q"]), up(inp["k"]), up(inp["v"])
+    O1, L1 = g.attn_fwd(q, k, v, mask_kind=MASK_CAUSAL)
+    buf = torch.empty(B * H * L * d + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(B, H, L, d)
+    assert out.data_ptr() % 32 == 16 and O1.data_ptr() % 32 == 0
+    O2, L2 = g.attn_fwd(q, k, v, mask_kind=MASK_CAUSAL, out=out)
+    g.check_device_status()
+    assert torch.equal(O1.view(torch.int16), O2.view(torch.int16))
+    assert torch.equal(L1.view(torch.int32), L2.view(torch.int32))
+
+
 def test_masked_keys_do_not_leak(cuda_lib):
     """Changing K and V at masked positions changes no output bit."""
     inp = make_attention_inputs(2, 2, 400, 400, 64, 64, seed=13)

@@ -76,6 +76,7 @@ struct AttnParams {
   float scale_log2;        // softmax scale * log2(e)
   __nv_bfloat16* O;
   long long o_stride_b, o_stride_h, o_stride_l;  // in elements
+  int o_v8;                // 1: O and its strides are 32-byte aligned (256-bit stores)
   float* LSE;              // [B,H,Lq] natural-log LSE, or nullptr
   int n_qblocks;           // ceil(Lq / 256)
   int n_items;             // B * H * n_qblocks
@@ -616,10 +617,16 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
           w[i] = zero_row ? 0u
                           : pack_bf16x2(__uint_as_float(ro[2 * i]) * inv_l,
                                         __uint_as_float(ro[2 * i + 1]) * inv_l);
+        // one row per thread: a 32-byte store fills whole sectors
+        if (p.o_v8) {
+          st_global_v8(orow + cc * 32, w);
+          st_global_v8(orow + cc * 32 + 16, w + 8);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          st_global_v4(orow + cc * 32 + i * 8, w[4 * i], w[4 * i + 1], w[4 * i + 2],
-                       w[4 * i + 3]);
+          for (int i = 0; i < 4; ++i)
+            st_global_v4(orow + cc * 32 + i * 8, w[4 * i], w[4 * i + 1], w[4 * i + 2],
+                         w[4 * i + 3]);
+        }
       }
     }
     if (p.LSE != nullptr && in_range) {

@@ -564,16 +564,18 @@ __device__ __forceinline__ void split_softmax_role(const int g, const AttnParams
         for (int i = 0; i < 32; ++i) r1[i] = 0u;
       }
       if (in_range && p.decode) {
+        // the workspace is 256-byte aligned and its rows are D floats: every
+        // 8-float group is 32-byte aligned
         float* prow = p.part_o + part * D + DH * g + cc * 32;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint32_t y[4];
+        for (int i = 0; i < 4; ++i) {
+          uint32_t y[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
+          for (int e = 0; e < 8; ++e)
             y[e] = zero_row ? 0u
-                            : __float_as_uint(__uint_as_float(r0[4 * i + e]) * f0 +
-                                              __uint_as_float(r1[4 * i + e]) * f1);
-          st_global_v4(prow + 4 * i, y[0], y[1], y[2], y[3]);
+                            : __float_as_uint(__uint_as_float(r0[8 * i + e]) * f0 +
+                                              __uint_as_float(r1[8 * i + e]) * f1);
+          st_global_v8(prow + 8 * i, y);
         }
       } else if (in_range) {
         uint32_t w[16];
@@ -584,10 +586,15 @@ __device__ __forceinline__ void split_softmax_role(const int g, const AttnParams
               __uint_as_float(r0[2 * i + 1]) * f0 + __uint_as_float(r1[2 * i + 1]) * f1;
           w[i] = zero_row ? 0u : pack_bf16x2(y0, y1);
         }
+        if (p.o_v8) {
+          st_global_v8(orow + cc * 32, w);
+          st_global_v8(orow + cc * 32 + 16, w + 8);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          st_global_v4(orow + cc * 32 + i * 8, w[4 * i], w[4 * i + 1], w[4 * i + 2],
-                       w[4 * i + 3]);
+          for (int i = 0; i < 4; ++i)
+            st_global_v4(orow + cc * 32 + i * 8, w[4 * i], w[4 * i + 1], w[4 * i + 2],
+                         w[4 * i + 3]);
+        }
       }
     }
     if (p.decode && in_range && g == 0) {

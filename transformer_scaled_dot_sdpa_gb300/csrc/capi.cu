@@ -180,6 +180,8 @@ attn_status_t run_attention(DeviceState* ds, const CUtensorMap& mq, const CUtens
   p.o_stride_b = osb;
   p.o_stride_h = osh;
   p.o_stride_l = osl;
+  // 256-bit O stores need every row start 32-byte aligned (the API asks for 16)
+  p.o_v8 = aligned(O, 32) && (osb * 2) % 32 == 0 && (osh * 2) % 32 == 0 && (osl * 2) % 32 == 0;
   p.LSE = LSE;
   p.status = ds->status;
   int schedule;
