@@ -193,6 +193,47 @@ attn_status_t attn_decode(const void* Q, const void* K, const void* V, int B, in
 size_t attn_decode_workspace_bytes(int B, int h, int h_kv, int Lq, int Lk, int d);
 
 /*
+ * attn_decode_host -- one decode step with host buffers for the step's own
+ * data and a key/value cache that stays on the device: it copies the Lq new
+ * query rows and the new tokens' key and value rows in, writes those rows
+ * into the cache, runs attn_decode over the cache and copies O and LSE out,
+ * all in order on `stream`.
+ *
+ *   Q        host bf16 [B, h, Lq, d]: the new tokens' query rows.
+ *   K_new, V_new  host bf16 [B, h_kv, Lq, d]: their key and value rows.
+ *   K_cache, V_cache  device bf16 [B, h_kv, Lk, d], 16-byte aligned; the
+ *            call writes row kv_len_b - Lq + i of (b, K/V head) with new row
+ *            i (rows whose position would be negative are dropped) and
+ *            reads the cache as attn_decode does.
+ *   kv_lens  host int32 [B] (required with ATTN_MASK_PADDING): valid keys
+ *            of each sequence after the new ones are appended, clamped to
+ *            [0, Lk].  Without padding every sequence holds Lk keys and the
+ *            new rows are the last Lq.
+ *   O, LSE   host bf16 [B, h, Lq, d] and float [B, h, Lq] (LSE may be NULL),
+ *            written when the stream reaches the end of the call.
+ *   workspace  device scratch of at least attn_decode_host_workspace_bytes()
+ *            bytes, 256-byte aligned: staging for the new rows, kv_lens, O,
+ *            LSE and attn_decode's own scratch.  Calls that share it must not
+ *            overlap.
+ *   mask_kind, scale, h_kv, d as for attn_decode.
+ *
+ * Host buffers may be pinned (the copies then run asynchronously) or
+ * pageable.  Lk = 0 returns ATTN_ERR_INVALID_ARG (no cache to append to).
+ * Other errors as for attn_decode.
+ */
+attn_status_t attn_decode_host(const void* Q, const void* K_new, const void* V_new, void* K_cache,
+                               void* V_cache, int B, int h, int h_kv, int Lq, int Lk, int d,
+                               int mask_kind, const int32_t* kv_lens, float scale, void* O,
+                               float* LSE, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
+ * attn_decode_host_workspace_bytes -- device scratch attn_decode_host needs
+ * for these sizes on the current device; 0 for empty or unsupported sizes.
+ */
+size_t attn_decode_host_workspace_bytes(int B, int h, int h_kv, int Lq, int Lk, int d);
+
+/*
  * attn_weights -- the attention matrix A for inspection of small problems.
  * The pages' reference snippets return A = softmax(Q K^T / sqrt(d_k) + M) next
  * to the output ("attention-mechanism" page, section "最小实现";

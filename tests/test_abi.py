@@ -146,6 +146,41 @@ def test_decode_validation(cdll):
     assert f(None, None, None, 0, 8, 2, 1, 64, 128, 4, None, 0.0, None, None, None, 0, None) == 0
 
 
+def test_decode_host_validation(cdll):
+    """attn_decode_host rejects bad shapes, a missing cache or workspace, a
+    padding mask without lengths and misaligned device buffers before any
+    CUDA call."""
+    f = cdll.attn_decode_host
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    f.restype = i
+    f.argtypes = [vp] * 5 + [i] * 7 + [vp, ctypes.c_float, vp, vp, vp, sz, vp]
+    ws = cdll.attn_decode_host_workspace_bytes
+    ws.restype = sz
+    ws.argtypes = [i] * 6
+    p = ctypes.c_void_p(0x1000)
+    INVALID, UNSUPPORTED, MISALIGNED = 1, 2, 3
+    BR = 4
+
+    def call(q=p, kc=p, vc=p, B=2, h=8, hkv=2, Lq=1, Lk=1000, d=128, mask=BR, kv=None,
+             out=p, work=p, nbytes=1 << 20):
+        return f(q, p, p, kc, vc, B, h, hkv, Lq, Lk, d, mask, kv, 0.0, out, None, work, nbytes,
+                 None)
+    assert call(hkv=3) == INVALID                      # h not a multiple of h_kv
+    assert call(d=96) == UNSUPPORTED
+    assert call(hkv=1, Lq=17) == UNSUPPORTED           # 8 x 17 rows > one tile
+    assert call(Lk=0) == INVALID                       # no cache to append to
+    assert call(kc=None) == INVALID
+    assert call(out=None) == INVALID
+    assert call(work=None) == INVALID
+    assert call(mask=BR | 2) == INVALID                # padding without kv_lens
+    assert call(mask=8) == INVALID                     # unknown mask bit
+    assert call(vc=ctypes.c_void_p(0x1008)) == MISALIGNED
+    assert call(work=ctypes.c_void_p(0x1080)) == MISALIGNED
+    assert call(B=0) == 0
+    assert ws(2, 8, 2, 1, 1000, 96) == 0
+    assert ws(2, 8, 3, 1, 1000, 128) == 0
+
+
 def test_probe_ex2_validation(cdll):
     f = cdll.attn_probe_ex2
     f.restype = ctypes.c_int

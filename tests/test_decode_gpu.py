@@ -103,3 +103,55 @@ def test_decode_timeout_is_reported_and_context_survives(cuda_lib):
     g.check_device_status()
     Or, Lr = oracle.attention(inp["q"], inp["k"], inp["v"], mask_kind=BR)
     compare_attention(down(O), L.cpu().numpy(), Or, Lr, "decode after timeout")
+
+
+HOST_CASES = [
+    # (B, h, h_kv, Lq, Lk, d, mask, kv_lens after the append)
+    (4, 16, 4, 1, 3000, 128, BR | MASK_PADDING, [3000, 1, 0, 1777]),
+    (2, 8, 8, 3, 1000, 64, BR, None),
+    (3, 32, 8, 2, 700, 128, BR | MASK_PADDING, [700, 2, 1]),
+]
+
+
+@pytest.mark.parametrize("case", HOST_CASES,
+                         ids=["x".join(map(str, c[:6])) + "-m%d" % c[6] for c in HOST_CASES])
+def test_decode_host_appends_then_attends(cuda_lib, case):
+    """attn_decode_host writes new row i of each (sequence, K/V head) at
+    position kv_len - Lq + i of the device caches (rows that would fall before
+    the start are dropped), then runs attn_decode: the caches equal the
+    expected append bit for bit, O / LSE equal attn_decode on the appended
+    caches bit for bit, and both match the oracle."""
+    import torch
+    g = cuda_lib
+    B, h, h_kv, Lq, Lk, d, mask, kv = case
+    inp = make_attention_inputs(B, h, Lq, Lk, d, d, seed=Lk + 11 * h, H_kv=h_kv)
+    new = make_attention_inputs(B, h_kv, Lq, Lq, d, d, seed=Lk + 13 * h)
+    k_new, v_new = new["k"], new["v"]  # [B, h_kv, Lq, d]
+    lens = kv if kv is not None else [Lk] * B
+    k_exp, v_exp = inp["k"].copy(), inp["v"].copy()
+    for b, n in enumerate(lens):
+        for i in range(Lq):
+            pos = min(max(n, 0), Lk) - Lq + i
+            if pos >= 0:
+                k_exp[b, :, pos] = k_new[b, :, i]
+                v_exp[b, :, pos] = v_new[b, :, i]
+
+    def host(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+            torch.bfloat16).pin_memory()
+    kc, vc = up(inp["k"]), up(inp["v"])
+    kv_host = torch.tensor(kv, dtype=torch.int32) if kv is not None else None
+    Oh, Lh = g.attn_decode_host(host(inp["q"]), host(k_new), host(v_new), kc, vc, mask_kind=mask,
+                                kv_lens=kv_host)
+    torch.cuda.current_stream().synchronize()
+    g.check_device_status()
+    assert np.array_equal(down(kc).view(np.uint32), down(up(k_exp)).view(np.uint32))
+    assert np.array_equal(down(vc).view(np.uint32), down(up(v_exp)).view(np.uint32))
+    kv_dev = kv_host.cuda() if kv_host is not None else None
+    Od, Ld = g.attn_decode(up(inp["q"]), up(k_exp), up(v_exp), mask_kind=mask, kv_lens=kv_dev)
+    g.check_device_status()
+    assert torch.equal(Oh.view(torch.int16), Od.cpu().view(torch.int16))
+    assert torch.equal(Lh.view(torch.int32), Ld.cpu().view(torch.int32))
+    kv_np = np.asarray(kv, dtype=np.int32) if kv is not None else None
+    Or, Lr = oracle.attention(inp["q"], k_exp, v_exp, mask_kind=mask, kv_lens=kv_np)
+    compare_attention(Oh.float().numpy(), Lh.numpy(), Or, Lr, "decode_host %s" % (case,))

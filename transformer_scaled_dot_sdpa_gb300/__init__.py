@@ -84,6 +84,11 @@ def _load():
                               vp]
     L.attn_decode_workspace_bytes.restype = sz
     L.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+    L.attn_decode_host.restype = i32
+    L.attn_decode_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32,
+                                   vp, vp, vp, sz, vp]
+    L.attn_decode_host_workspace_bytes.restype = sz
+    L.attn_decode_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     L.attn_weights.restype = i32
     L.attn_weights.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp]
     L.mha_layer_workspace_bytes.restype = sz
@@ -232,6 +237,54 @@ def attn_fwd_host(q, k, v, mask_kind=MASK_NONE, kv_lens=None, scale=None, out=No
                            _ptr(kv_lens), float(scale) if scale else 0.0, _ptr(out), _ptr(lse),
                            _ptr(workspace), workspace.numel(), _stream_handle(stream))
     _check(st, "attn_fwd_host")
+    return out, lse
+
+
+def attn_decode_host_workspace_bytes(B, h, h_kv, Lq, Lk, d):
+    return int(lib.attn_decode_host_workspace_bytes(int(B), int(h), int(h_kv), int(Lq), int(Lk),
+                                                    int(d)))
+
+
+def attn_decode_host(q, k_new, v_new, k_cache, v_cache, mask_kind=MASK_CAUSAL_BOTTOM_RIGHT,
+                     kv_lens=None, scale=None, out=None, lse=None, return_lse=True,
+                     workspace=None, stream=None):
+    """One decode step with host buffers: the new query rows ``q`` [B, h, Lq, d]
+    and the new tokens' ``k_new`` / ``v_new`` [B, h_kv, Lq, d] (CPU bf16
+    tensors, pinned for asynchronous copies) go in; the new K/V rows are
+    written into the device caches ``k_cache`` / ``v_cache`` [B, h_kv, Lk, d]
+    at positions kv_len - Lq .. kv_len - 1 (``kv_lens``: int32 CPU tensor of
+    the lengths after the append; without it every cache is full); then
+    attn_decode runs over the caches and O / LSE come back in CPU tensors,
+    valid once ``stream`` has been synchronised."""
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new")):
+        _host_tensor(t, n, torch.bfloat16)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _dev_tensor(t, n, torch.bfloat16)
+    B, h, Lq, d = q.shape
+    h_kv, Lk = k_cache.shape[1], k_cache.shape[2]
+    if (tuple(k_cache.shape) != (B, h_kv, Lk, d) or tuple(v_cache.shape) != (B, h_kv, Lk, d)
+            or tuple(k_new.shape) != (B, h_kv, Lq, d) or tuple(v_new.shape) != (B, h_kv, Lq, d)):
+        raise ValueError("q / new rows / cache shapes do not match")
+    if out is None:
+        out = torch.empty((B, h, Lq, d), dtype=torch.bfloat16).pin_memory()
+    _host_tensor(out, "out", torch.bfloat16)
+    if tuple(out.shape) != (B, h, Lq, d):
+        raise ValueError("out has the wrong shape")
+    if lse is None and return_lse:
+        lse = torch.empty((B, h, Lq), dtype=torch.float32).pin_memory()
+    if lse is not None:
+        _host_tensor(lse, "lse", torch.float32)
+    if kv_lens is not None:
+        _host_tensor(kv_lens, "kv_lens", torch.int32)
+    need = attn_decode_host_workspace_bytes(B, h, h_kv, Lq, Lk, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=k_cache.device)
+    _dev_tensor(workspace, "workspace", torch.uint8)
+    st = lib.attn_decode_host(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), B,
+                              h, h_kv, Lq, Lk, d, int(mask_kind), _ptr(kv_lens),
+                              float(scale) if scale else 0.0, _ptr(out), _ptr(lse),
+                              _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(st, "attn_decode_host")
     return out, lse
 
 

@@ -13,6 +13,7 @@
 #include "attn_fwd_kernel.cuh"
 #include "attn_fwd_split_kernel.cuh"
 #include "attn_weights_kernel.cuh"
+#include "kv_append_kernel.cuh"
 #include "gemm_kernel.cuh"
 #include "probe_kernel.cuh"
 
@@ -645,25 +646,9 @@ size_t decode_part_o_bytes(long long rows, int n_chunks, int d) {
   return (static_cast<size_t>(rows) * n_chunks * d * 4 + 255) / 256 * 256;
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t attn_decode_workspace_bytes(int B, int h, int h_kv, int Lq, int Lk, int d) {
-  if (B <= 0 || h <= 0 || h_kv <= 0 || Lq <= 0 || Lk <= 0 || (d != 64 && d != 128)) return 0;
-  DeviceState* ds = nullptr;
-  if (device_state(&ds, nullptr) != ATTN_OK) return 0;
-  const DecodePlan plan = decode_plan(ds->num_sms, B, h_kv, Lk);
-  const long long rows = static_cast<long long>(B) * h * Lq;
-  return decode_part_o_bytes(rows, plan.n_chunks, d) +
-         static_cast<size_t>(rows) * plan.n_chunks * 4 * sizeof(float);
-}
-
-attn_status_t attn_decode(const void* Q, const void* K, const void* V, int B, int h, int h_kv,
-                          int Lq, int Lk, int d, int mask_kind, const int32_t* kv_lens,
-                          float scale, void* O, float* LSE, void* workspace,
-                          size_t workspace_bytes, void* stream) {
-  // ---- host-side validation (no CUDA call before this point) ----
+// Argument checks shared by attn_decode and attn_decode_host (no CUDA call).
+attn_status_t check_decode_shape(int B, int h, int h_kv, int Lq, int Lk, int d, int mask_kind,
+                                 float scale) {
   if (B < 0 || h < 0 || Lq < 0 || Lk < 0) return ATTN_ERR_INVALID_ARG;
   if (h_kv < 1 || (h > 0 && h % h_kv != 0)) return ATTN_ERR_INVALID_ARG;
   if ((mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_PADDING | ATTN_MASK_CAUSAL_BOTTOM_RIGHT)) != 0)
@@ -674,31 +659,56 @@ attn_status_t attn_decode(const void* Q, const void* K, const void* V, int B, in
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (h > 0 && static_cast<long long>(h / h_kv) * Lq > gb300::SPLIT_ROWS)
     return ATTN_ERR_UNSUPPORTED;  // the query rows of one K/V head fill one 128-row tile
-  if (static_cast<long long>(B) * h * Lq >= (1ll << 31) || static_cast<long long>(B) * h_kv *
-                                                               ((static_cast<long long>(Lk) + 127) / 128) >= (1ll << 31))
+  if (static_cast<long long>(B) * h * Lq >= (1ll << 31) ||
+      static_cast<long long>(B) * h_kv * ((static_cast<long long>(Lk) + 127) / 128) >= (1ll << 31))
     return ATTN_ERR_UNSUPPORTED;
-  if (B == 0 || h == 0 || Lq == 0) return ATTN_OK;
-  if (!O) return ATTN_ERR_INVALID_ARG;
-  if ((mask_kind & ATTN_MASK_PADDING) && !kv_lens) return ATTN_ERR_INVALID_ARG;
-  if (Lk > 0 && (!Q || !K || !V || !workspace)) return ATTN_ERR_INVALID_ARG;
-  if (!aligned(O, 16) || (LSE && !aligned(LSE, 4)) || (kv_lens && !aligned(kv_lens, 4)))
-    return ATTN_ERR_MISALIGNED;
-  if (Lk > 0 && (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) ||
-                 !aligned(workspace, 256)))
-    return ATTN_ERR_MISALIGNED;
+  return ATTN_OK;
+}
 
-  DeviceState* ds = nullptr;
-  attn_status_t st = device_state(&ds, nullptr);
-  if (st != ATTN_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+// attn_decode_host's workspace: staging for the new query rows and K/V rows,
+// kv_lens, O and LSE; attn_decode's own workspace follows at `total`.
+struct DecodeHostLayout {
+  size_t q, knew, vnew, kv, o, lse, total;
+};
+
+DecodeHostLayout decode_host_layout(int B, int h, int h_kv, int Lq, int d) {
+  DecodeHostLayout l;
+  size_t off = 0;
+  l.q = off;
+  off = align256(off + static_cast<size_t>(B) * h * Lq * d * 2);
+  l.knew = off;
+  off = align256(off + static_cast<size_t>(B) * h_kv * Lq * d * 2);
+  l.vnew = off;
+  off = align256(off + static_cast<size_t>(B) * h_kv * Lq * d * 2);
+  l.kv = off;
+  off = align256(off + static_cast<size_t>(B) * 4);
+  l.o = off;
+  off = align256(off + static_cast<size_t>(B) * h * Lq * d * 2);
+  l.lse = off;
+  off = align256(off + static_cast<size_t>(B) * h * Lq * 4);
+  l.total = off;
+  return l;
+}
+
+// Split-KV decode on validated device buffers: the split kernel over
+// (sequence, K/V head, key chunk) items, then the merge of the chunks.
+attn_status_t decode_device(DeviceState* ds, const void* Q, const void* K, const void* V, int B,
+                            int h, int h_kv, int Lq, int Lk, int d, int mask_kind,
+                            const int32_t* kv_lens, float scale, void* O, float* LSE,
+                            uint8_t* ws, cudaStream_t s);
+
+
+attn_status_t decode_device(DeviceState* ds, const void* Q, const void* K, const void* V, int B,
+                            int h, int h_kv, int Lq, int Lk, int d, int mask_kind,
+                            const int32_t* kv_lens, float scale, void* O, float* LSE,
+                            uint8_t* ws, cudaStream_t s) {
+  attn_status_t st;
   if (Lk == 0) {
     const long long osl = d, osh = static_cast<long long>(Lq) * d, osb = osh * h;
     gb300::attn_empty_keys_kernel<<<256, 256, 0, s>>>(static_cast<__nv_bfloat16*>(O), osb, osh,
                                                      osl, LSE, B, h, Lq, d);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
-  if (workspace_bytes < attn_decode_workspace_bytes(B, h, h_kv, Lq, Lk, d))
-    return ATTN_ERR_INVALID_ARG;
   const DecodePlan plan = decode_plan(ds->num_sms, B, h_kv, Lk);
   const long long rows = static_cast<long long>(B) * h * Lq;
 
@@ -732,7 +742,6 @@ attn_status_t attn_decode(const void* Q, const void* K, const void* V, int B, in
   p.n_chunks = plan.n_chunks;
   p.n_qblocks = 1;
   p.n_items = static_cast<int>(static_cast<long long>(B) * h_kv * plan.n_chunks);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.part_o = reinterpret_cast<float*>(ws);
   p.part_ml = reinterpret_cast<float*>(ws + decode_part_o_bytes(rows, plan.n_chunks, d));
   st = d == 64 ? launch_attn<64, ATTN_SCHEDULE_SPLIT_KEYS>(ds, mq, mk, mv, p, s)
@@ -746,6 +755,111 @@ attn_status_t attn_decode(const void* Q, const void* K, const void* V, int B, in
     gb300::attn_decode_combine_kernel<128><<<grid, 128, 0, s>>>(
         p.part_o, p.part_ml, plan.n_chunks, rows, static_cast<__nv_bfloat16*>(O), LSE);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_decode_workspace_bytes(int B, int h, int h_kv, int Lq, int Lk, int d) {
+  if (B <= 0 || h <= 0 || h_kv <= 0 || Lq <= 0 || Lk <= 0 || (d != 64 && d != 128)) return 0;
+  DeviceState* ds = nullptr;
+  if (device_state(&ds, nullptr) != ATTN_OK) return 0;
+  const DecodePlan plan = decode_plan(ds->num_sms, B, h_kv, Lk);
+  const long long rows = static_cast<long long>(B) * h * Lq;
+  return decode_part_o_bytes(rows, plan.n_chunks, d) +
+         static_cast<size_t>(rows) * plan.n_chunks * 4 * sizeof(float);
+}
+
+attn_status_t attn_decode(const void* Q, const void* K, const void* V, int B, int h, int h_kv,
+                          int Lq, int Lk, int d, int mask_kind, const int32_t* kv_lens,
+                          float scale, void* O, float* LSE, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  // ---- host-side validation (no CUDA call before this point) ----
+  attn_status_t st = check_decode_shape(B, h, h_kv, Lq, Lk, d, mask_kind, scale);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || h == 0 || Lq == 0) return ATTN_OK;
+  if (!O) return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ATTN_MASK_PADDING) && !kv_lens) return ATTN_ERR_INVALID_ARG;
+  if (Lk > 0 && (!Q || !K || !V || !workspace)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(O, 16) || (LSE && !aligned(LSE, 4)) || (kv_lens && !aligned(kv_lens, 4)))
+    return ATTN_ERR_MISALIGNED;
+  if (Lk > 0 && (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) ||
+                 !aligned(workspace, 256)))
+    return ATTN_ERR_MISALIGNED;
+
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds, nullptr)) != ATTN_OK) return st;
+  if (Lk > 0 && workspace_bytes < attn_decode_workspace_bytes(B, h, h_kv, Lq, Lk, d))
+    return ATTN_ERR_INVALID_ARG;
+  return decode_device(ds, Q, K, V, B, h, h_kv, Lq, Lk, d, mask_kind, kv_lens, scale, O, LSE,
+                       static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_decode_host_workspace_bytes(int B, int h, int h_kv, int Lq, int Lk, int d) {
+  if (check_decode_shape(B, h, h_kv, Lq, Lk, d, 0, 0.f) != ATTN_OK || B == 0 || h == 0 ||
+      Lq == 0 || Lk == 0)
+    return 0;
+  const size_t dec = attn_decode_workspace_bytes(B, h, h_kv, Lq, Lk, d);
+  if (dec == 0) return 0;
+  return decode_host_layout(B, h, h_kv, Lq, d).total + align256(dec);
+}
+
+attn_status_t attn_decode_host(const void* Q, const void* K_new, const void* V_new, void* K_cache,
+                               void* V_cache, int B, int h, int h_kv, int Lq, int Lk, int d,
+                               int mask_kind, const int32_t* kv_lens, float scale, void* O,
+                               float* LSE, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  // ---- host-side validation (no CUDA call before this point) ----
+  attn_status_t st = check_decode_shape(B, h, h_kv, Lq, Lk, d, mask_kind, scale);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || h == 0 || Lq == 0) return ATTN_OK;
+  if (Lk == 0) return ATTN_ERR_INVALID_ARG;  // the new rows need a cache to go into
+  if (!Q || !K_new || !V_new || !K_cache || !V_cache || !O || !workspace)
+    return ATTN_ERR_INVALID_ARG;
+  if ((mask_kind & ATTN_MASK_PADDING) && !kv_lens) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(K_cache, 16) || !aligned(V_cache, 16) || !aligned(workspace, 256))
+    return ATTN_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds, nullptr)) != ATTN_OK) return st;
+  if (workspace_bytes < attn_decode_host_workspace_bytes(B, h, h_kv, Lq, Lk, d))
+    return ATTN_ERR_INVALID_ARG;
+
+  const DecodeHostLayout lay = decode_host_layout(B, h, h_kv, Lq, d);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t q_bytes = static_cast<size_t>(B) * h * Lq * d * 2;
+  const size_t kv_bytes = static_cast<size_t>(B) * h_kv * Lq * d * 2;
+  const bool padding = (mask_kind & ATTN_MASK_PADDING) != 0;
+  int32_t* dkv = padding ? reinterpret_cast<int32_t*>(ws + lay.kv) : nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // inputs in: four copies on the caller's stream
+  cudaError_t e = cudaMemcpyAsync(ws + lay.q, Q, q_bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(ws + lay.knew, K_new, kv_bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(ws + lay.vnew, V_new, kv_bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && padding)
+    e = cudaMemcpyAsync(dkv, kv_lens, static_cast<size_t>(B) * 4, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  // the new rows into the cache, then attention over it
+  {
+    const long long pieces = static_cast<long long>(B) * h_kv * Lq * (d / 8);
+    const unsigned grid =
+        static_cast<unsigned>(pieces / 256 + 1 < 4 * ds->num_sms ? pieces / 256 + 1 : 4 * ds->num_sms);
+    gb300::kv_append_kernel<<<grid, 256, 0, s>>>(
+        reinterpret_cast<const uint4*>(ws + lay.knew), reinterpret_cast<const uint4*>(ws + lay.vnew),
+        static_cast<uint4*>(K_cache), static_cast<uint4*>(V_cache), dkv, B, h_kv, Lq, Lk, d / 8);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  float* dL = LSE ? reinterpret_cast<float*>(ws + lay.lse) : nullptr;
+  st = decode_device(ds, ws + lay.q, K_cache, V_cache, B, h, h_kv, Lq, Lk, d, mask_kind, dkv,
+                     scale, ws + lay.o, dL, ws + lay.total, s);
+  if (st != ATTN_OK) return st;
+  // outputs out
+  e = cudaMemcpyAsync(O, ws + lay.o, q_bytes, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && LSE)
+    e = cudaMemcpyAsync(LSE, dL, static_cast<size_t>(B) * h * Lq * 4, cudaMemcpyDeviceToHost, s);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status_t attn_weights(const void* Q, const void* K, const float* LSE, int B, int h,
