@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -36,8 +37,9 @@ struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   unsigned int* status = nullptr;
-  bool attn_attr[4] = {false, false, false, false};
-  bool gemm_attr = false;
+  // one-time kernel set-up, done under g_mutex and published by the flags
+  std::atomic<bool> attn_attr[4] = {false, false, false, false};
+  std::atomic<bool> gemm_attr{false};
   int gemm_pairs = 0;  // CTA pairs of the GEMM kernel resident at once
   // attn_fwd_host: copy-in, copy-out and a second compute stream, and the
   // events that order them (created on first use)
@@ -138,7 +140,8 @@ attn_status_t launch_attn(DeviceState* ds, const CUtensorMap& mq, const CUtensor
   const int smem = split ? gb300::SplitLayout<D>::SMEM_BYTES : gb300::AttnLayout<D>::SMEM_BYTES;
   void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, gb300::AttnParams) =
       split ? gb300::attn_fwd_split_kernel<D> : gb300::attn_fwd_kernel<D>;
-  if (!ds->attn_attr[attr_idx]) {
+  if (!ds->attn_attr[attr_idx].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_mutex);
     // The kernels hand registers between warpgroups (setmaxnreg); the split
     // adds up to exactly ATTN_THREADS x ATTN_REGS_AT_LAUNCH, so a build with a
     // different launch register count could wait forever: refuse it.
@@ -149,7 +152,7 @@ attn_status_t launch_attn(DeviceState* ds, const CUtensorMap& mq, const CUtensor
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return ATTN_ERR_CUDA;
-    ds->attn_attr[attr_idx] = true;
+    ds->attn_attr[attr_idx].store(true, std::memory_order_release);
   }
   const int grid = p.n_items < ds->num_sms ? p.n_items : ds->num_sms;
   kernel<<<grid, gb300::ATTN_THREADS, smem, stream>>>(mq, mk, mv, p);
@@ -232,7 +235,8 @@ attn_status_t run_gemm(DeviceState* ds, const void* A, const void* Bm, void* C, 
   if ((st = map_2d(&ma, A, M, K, gb300::GEMM_BK, gb300::GEMM_BM_CTA)) != ATTN_OK) return st;
   if ((st = map_2d(&mb, Bm, K, N, 64, gb300::GEMM_BK)) != ATTN_OK) return st;
   if ((st = map_2d(&mc, C, M, N, 64, 32)) != ATTN_OK) return st;  // epilogue store boxes
-  if (!ds->gemm_attr) {
+  if (!ds->gemm_attr.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_mutex);
     if (cudaFuncSetAttribute(gb300::gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              gb300::GemmLayout::SMEM_BYTES) != cudaSuccess)
       return ATTN_ERR_CUDA;
@@ -248,7 +252,7 @@ attn_status_t run_gemm(DeviceState* ds, const void* A, const void* Bm, void* C, 
         clusters < 1)
       return ATTN_ERR_CUDA;
     ds->gemm_pairs = clusters;
-    ds->gemm_attr = true;
+    ds->gemm_attr.store(true, std::memory_order_release);
   }
   gb300::GemmParams p;
   std::memset(&p, 0, sizeof p);
