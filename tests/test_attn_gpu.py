@@ -161,6 +161,21 @@ def test_large_workloads_sampled(cuda_lib, name, rows_per_head):
     assert np.array_equal(O[:, :, 0, :], bf16_to_f32(inp["v"][:, :, 0, :]))
 
 
+def test_longest_sequence_sampled(cuda_lib):
+    """The longest sequence the suite takes: one sequence of 131072 tokens, two
+    heads, causal, d = 128 (TMA row coordinates up to 2^17, 512 row blocks per
+    head, diagonal tiles 1024 key tiles deep).  A stratified sample of rows of
+    both heads, the first and last included, against the oracle."""
+    B, H, L, d = 1, 2, 131072, 128
+    inp = make_attention_inputs(B, H, L, L, d, d, seed=131)
+    O, Lse = _run(cuda_lib, inp, MASK_CAUSAL)
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(Lse))
+    rows_in_head = sample_rows(L, 32, seed=131)
+    flat = np.concatenate([bh * L + rows_in_head for bh in range(B * H)])
+    Or, Lr = oracle.attention(inp["q"], inp["k"], inp["v"], mask_kind=MASK_CAUSAL, rows=flat)
+    compare_attention(O.reshape(-1, d)[flat], Lse.reshape(-1)[flat], Or, Lr, "L = 131072")
+
+
 _ORACLE_CACHE = {}
 
 
