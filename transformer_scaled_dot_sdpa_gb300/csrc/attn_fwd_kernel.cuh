@@ -84,14 +84,14 @@ struct AttnParams {
   unsigned long long wait_limit_ns;
   long long debug_skip_kv_load;  // test hook: skip this running K-tile load (-1: none)
   // split-KV decode (attn_fwd_split_kernel only; decode == 0 everywhere else):
-  // an item is (b, K/V head, chunk of kv_chunk keys); its Q tile packs the
-  // q_rows = kv_group * Lq query rows of the heads that share the K/V head,
-  // and its epilogue writes an unnormalised partial result per chunk
+  // an item is the part of one (b, K/V head) pair's key tiles that falls in
+  // the CTA's share of all pairs' tiles; its Q tile packs the q_rows =
+  // kv_group * Lq query rows of the heads that share the K/V head, and its
+  // epilogue writes an unnormalised partial result to one of the row's slots
   int decode;
   int q_rows;
-  int kv_chunk;            // multiple of 128
-  int n_chunks;
-  float* part_o;           // [B*H*Lq][n_chunks][D]: w_0 O_0 + w_1 O_1 of the chunk
+  int n_chunks;            // partial-result slots per query row
+  float* part_o;           // [B*H*Lq][n_chunks][D]: w_0 O_0 + w_1 O_1 of the item
   float* part_ml;          // [B*H*Lq][n_chunks][4]: m (log2 units), l, lb, 0
 };
 

@@ -43,50 +43,103 @@ constexpr int SPLIT_ROWS = 128;  // query rows per work item
 struct SplitItem {
   int b, h, kvh, row0, nkv, kv_len, kv_len_raw;
   int k0;     // first key of the item's key range
-  int chunk;  // decode: chunk index; qrow: flat index of the first packed Q row
-  int qrow;
+  int chunk;  // decode: slot of the item's partial result among its pair's
+  int qrow;   // decode: flat index of the first packed Q row
 };
 
-// Item k of this CTA, dealt in a boustrophedon order like attn_get_item.
-// Attention: one (b, h, 128-row query tile), heaviest first.  Decode: one
-// (b, K/V head, key chunk), chunk-major.
+// Split-KV decode plan, computed alike by every role of every CTA and by the
+// combine kernel from kv_lens: the visible key tiles of all (sequence, K/V
+// head) pairs, laid end to end in pair order, are cut into gridDim.x ranges of
+// ceil(T / gridDim.x) tiles.  CTA c takes range c; each part of a pair inside
+// the range is one work item, whose partial result goes to slot
+// c - (first CTA of the pair).  Every CTA gets the same number of key tiles
+// (within one), whatever the cache lengths.
+__device__ __forceinline__ int decode_seq_tiles(const AttnParams& p, int b) {
+  int len = p.Lk;
+  if (p.mask_kind & ATTN_MASK_PADDING_BIT) {
+    const int raw = p.kv_lens[b];
+    len = raw < 0 ? 0 : (raw > p.Lk ? p.Lk : raw);
+  }
+  // keys the last query row may see bound those of every row of the pair
+  if (p.mask_kind & ATTN_MASK_CAUSAL_BIT) len = min(len, max(p.Lq + p.causal_offset, 0));
+  return (len + ATTN_BLOCK_N - 1) / ATTN_BLOCK_N;
+}
+
+struct DecodeSplit {
+  long long total;  // key tiles of all pairs
+  long long share;  // key tiles per CTA range
+};
+
+__device__ __forceinline__ DecodeSplit decode_split(const AttnParams& p, int grid) {
+  const int hkv = p.H / p.kv_group;
+  long long total = 0;
+  for (int b = 0; b < p.B; ++b) total += static_cast<long long>(hkv) * decode_seq_tiles(p, b);
+  return {total, total > 0 ? (total + grid - 1) / grid : 0};
+}
+
+// Item k of this CTA.  Attention: one (b, h, 128-row query tile), heaviest
+// first, dealt in a boustrophedon order like attn_get_item.  Decode: the k-th
+// pair part of this CTA's range of key tiles (see decode_split).
 __device__ __forceinline__ bool split_get_item(const AttnParams& p, int k, SplitItem& it) {
   const int G = static_cast<int>(gridDim.x);
   const int c = static_cast<int>(blockIdx.x);
-  const long long w = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
-  if (w >= p.n_items) return false;
   if (p.decode) {
     const int hkv = p.H / p.kv_group;
-    const int pairs = p.B * hkv;
-    it.chunk = static_cast<int>(w / pairs);
-    const int bk = static_cast<int>(w - static_cast<long long>(it.chunk) * pairs);
-    it.b = bk / hkv;
-    it.kvh = bk - it.b * hkv;
-    it.h = it.kvh * p.kv_group;
-#ifdef GB300_CHECKED
-    if (!check_ok(it.b >= 0 && it.b < p.B && it.kvh >= 0 && it.kvh < hkv && it.chunk >= 0 &&
-                      it.chunk < p.n_chunks,
-                  CHECK_ITEM))
-      return false;
-#endif
-    it.qrow = (it.b * p.H + it.h) * p.Lq;
-    int kv_len = p.Lk;
-    it.kv_len_raw = p.Lk;
-    if (p.mask_kind & ATTN_MASK_PADDING_BIT) {
-      const int raw = p.kv_lens[it.b];
-      it.kv_len_raw = raw;
-      kv_len = raw < 0 ? 0 : (raw > p.Lk ? p.Lk : raw);
+    const DecodeSplit ds = decode_split(p, G);
+    const long long lo = static_cast<long long>(c) * ds.share;
+    const long long hi = min(ds.total, lo + ds.share);
+    if (lo >= hi) return false;
+    // the sequence holding tile lo (sequences without visible keys hold none)
+    long long cum = 0;  // first tile of sequence b
+    int b = 0, nt = 0;
+    for (; b < p.B; ++b) {
+      nt = decode_seq_tiles(p, b);
+      if (lo < cum + static_cast<long long>(hkv) * nt) break;
+      cum += static_cast<long long>(hkv) * nt;
     }
-    it.kv_len = kv_len;
-    it.row0 = 0;
-    it.k0 = it.chunk * p.kv_chunk;
-    // keys the last query row may see bound those of every row of the item
-    int lim = kv_len;
-    if (p.mask_kind & ATTN_MASK_CAUSAL_BIT) lim = min(lim, max(p.Lq + p.causal_offset, 0));
-    const int hi = min(lim, it.k0 + p.kv_chunk);
-    it.nkv = hi > it.k0 ? (hi - it.k0 + ATTN_BLOCK_N - 1) / ATTN_BLOCK_N : 0;
-    return true;
+    long long x = lo;
+    for (int i = 0;; ++i) {
+      if (b >= p.B || nt <= 0) return false;  // unreachable while x < hi
+      const long long off = x - cum;
+      const int kvh = static_cast<int>(off / nt);
+      const int t0 = static_cast<int>(off - static_cast<long long>(kvh) * nt);
+      const long long pair0 = cum + static_cast<long long>(kvh) * nt;  // first tile of the pair
+      const long long end = min(pair0 + nt, hi);
+      if (i == k) {
+        it.b = b;
+        it.kvh = kvh;
+        it.h = kvh * p.kv_group;
+        it.chunk = static_cast<int>(c - pair0 / ds.share);
+#ifdef GB300_CHECKED
+        if (!check_ok(it.b < p.B && it.kvh < hkv && it.chunk >= 0 && it.chunk < p.n_chunks,
+                      CHECK_ITEM))
+          return false;
+#endif
+        it.qrow = (it.b * p.H + it.h) * p.Lq;
+        int kv_len = p.Lk;
+        it.kv_len_raw = p.Lk;
+        if (p.mask_kind & ATTN_MASK_PADDING_BIT) {
+          const int raw = p.kv_lens[it.b];
+          it.kv_len_raw = raw;
+          kv_len = raw < 0 ? 0 : (raw > p.Lk ? p.Lk : raw);
+        }
+        it.kv_len = kv_len;
+        it.row0 = 0;
+        it.k0 = t0 * ATTN_BLOCK_N;
+        it.nkv = static_cast<int>(end - x);
+        return true;
+      }
+      x = end;
+      if (x >= hi) return false;
+      if (x >= cum + static_cast<long long>(hkv) * nt) {  // on to the next sequence with tiles
+        cum += static_cast<long long>(hkv) * nt;
+        for (++b; b < p.B && (nt = decode_seq_tiles(p, b)) == 0; ++b) {
+        }
+      }
+    }
   }
+  const long long w = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
+  if (w >= p.n_items) return false;
   it.k0 = 0;
   it.chunk = 0;
   it.qrow = 0;
@@ -702,23 +755,38 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
 // the identity by which the online softmax merges partial results
 // ("Self-Attention 机制", Softmax 的数值稳定性与 Online Softmax).  Rows whose
 // every chunk is empty (padded or without keys) get O = 0 and LSE = -inf.
-// Lane c reads the (m, l, lb) of chunks c, c + 32, ... and the warp reduces
+// The row's pair has one partial per CTA range that overlaps its key tiles
+// (decode_split, recomputed here from kv_lens): slots 0 .. last - first.
+// Lane c reads the (m, l, lb) of slots c, c + 32, ... and the warp reduces
 // them with shuffles, so the statistics cost one round trip to memory, not
-// one per chunk.  Then lane l accumulates output columns l, l + 32, ... over
-// the chunks in chunk order, with several chunks' loads in flight.
+// one per slot.  Then lane l accumulates output columns l, l + 32, ... over
+// the slots in slot order, with several slots' loads in flight.
 template <int D>
 __global__ void __launch_bounds__(128)
-    attn_decode_combine_kernel(const float* __restrict__ part_o,
-                               const float* __restrict__ part_ml, int n_chunks, long long rows,
+    attn_decode_combine_kernel(const AttnParams p, int grid, long long rows,
                                __nv_bfloat16* __restrict__ O, float* __restrict__ LSE) {
   constexpr int PER = D / 32;
   constexpr unsigned FULL = 0xffffffffu;
   const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31u);
   if (row >= rows) return;  // uniform over the warp
-  const float4* ml = reinterpret_cast<const float4*>(part_ml + row * n_chunks * 4);
+  // the row's pair and the slots of its partial results
+  const int hkv = p.H / p.kv_group;
+  const int b = static_cast<int>(row / (static_cast<long long>(p.H) * p.Lq));
+  const int kvh = static_cast<int>((row / p.Lq) % p.H) / p.kv_group;
+  const DecodeSplit ds = decode_split(p, grid);
+  long long cum = 0;
+  for (int i = 0; i < b; ++i) cum += static_cast<long long>(hkv) * decode_seq_tiles(p, i);
+  const int nt = decode_seq_tiles(p, b);
+  int n_slots = 0;
+  if (nt > 0) {
+    const long long pair0 = cum + static_cast<long long>(kvh) * nt;
+    n_slots = static_cast<int>((pair0 + nt - 1) / ds.share - pair0 / ds.share) + 1;
+  }
+  const float* part_o = p.part_o + row * p.n_chunks * D;
+  const float4* ml = reinterpret_cast<const float4*>(p.part_ml + row * p.n_chunks * 4);
   float mm = -INFINITY;
-  for (int c = lane; c < n_chunks; c += 32) mm = fmaxf(mm, ml[c].x);
+  for (int c = lane; c < n_slots; c += 32) mm = fmaxf(mm, ml[c].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(FULL, mm, o));
   float acc[PER];
@@ -726,9 +794,9 @@ __global__ void __launch_bounds__(128)
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
   float l = 0.f, lb = 0.f;
   if (mm != -INFINITY) {
-    for (int c0 = 0; c0 < n_chunks; c0 += 32) {
-      float w = 0.f;  // weight of chunk c0 + lane; 0 for an empty chunk
-      if (c0 + lane < n_chunks) {
+    for (int c0 = 0; c0 < n_slots; c0 += 32) {
+      float w = 0.f;  // weight of slot c0 + lane; 0 for an empty partial
+      if (c0 + lane < n_slots) {
         const float4 v = ml[c0 + lane];
         if (v.x != -INFINITY) {
           w = ex2_approx(v.x - mm);
@@ -736,8 +804,8 @@ __global__ void __launch_bounds__(128)
           lb += w * v.z;
         }
       }
-      const int nc = min(32, n_chunks - c0);
-      const float* po = part_o + (row * n_chunks + c0) * D + lane;
+      const int nc = min(32, n_slots - c0);
+      const float* po = part_o + static_cast<long long>(c0) * D + lane;
 #pragma unroll 4
       for (int j = 0; j < nc; ++j) {
         const float wj = __shfl_sync(FULL, w, j);

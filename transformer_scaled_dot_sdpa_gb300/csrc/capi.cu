@@ -625,25 +625,13 @@ attn_status_t attn_fwd_host(const void* Q, const void* K, const void* V, int B, 
 
 namespace {
 
-// Split-KV decode: chunk the keys into about `per_sm` work items per SM over
-// the B * h_kv (sequence, K/V head) pairs.  per_sm follows a sweep on GB300
-// (GQA, d = 128): one item per SM was best with 8-16 pairs (4.7 TB/s at 8
-// pairs, 3.0 with six); with 32-64 pairs three to five were best and four
-// was within 6% of the best everywhere (5.4 TB/s, 3.9-4.9 with one), also
-// with cache lengths that vary between sequences.
-struct DecodePlan {
-  int n_chunks;
-  int kv_chunk;  // keys per chunk, a multiple of 128
-};
-
-DecodePlan decode_plan(int num_sms, int B, int h_kv, int Lk) {
-  const long long pairs = static_cast<long long>(B) * h_kv;
-  const long long max_chunks = (static_cast<long long>(Lk) + 127) / 128;
-  const long long per_sm = pairs < 24 ? 1 : 4;
-  long long n = (per_sm * num_sms + pairs - 1) / pairs;
-  n = n < 1 ? 1 : (n > max_chunks ? max_chunks : n);
-  const int chunk = static_cast<int>(((Lk + n - 1) / n + 127) / 128 * 128);
-  return {static_cast<int>((Lk + chunk - 1) / chunk), chunk};
+// Split-KV decode: the kernel cuts all (sequence, K/V head) pairs' key tiles
+// into one equal range per CTA (decode_split in attn_fwd_split_kernel.cuh), so
+// a pair's tiles are spread over at most min(CTAs, its tiles + 1) ranges: the
+// partial-result slots each query row needs.
+int decode_slots(int grid, int Lk) {
+  const long long tiles = (static_cast<long long>(Lk) + gb300::ATTN_BLOCK_N - 1) / gb300::ATTN_BLOCK_N;
+  return static_cast<int>(tiles + 1 < grid ? tiles + 1 : grid);
 }
 
 size_t decode_part_o_bytes(long long rows, int n_chunks, int d) {
@@ -713,7 +701,8 @@ attn_status_t decode_device(DeviceState* ds, const void* Q, const void* K, const
                                                      osl, LSE, B, h, Lq, d);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
-  const DecodePlan plan = decode_plan(ds->num_sms, B, h_kv, Lk);
+  const int grid = ds->num_sms;
+  const int slots = decode_slots(grid, Lk);
   const long long rows = static_cast<long long>(B) * h * Lq;
 
   CUtensorMap mq, mk, mv;
@@ -742,22 +731,21 @@ attn_status_t decode_device(DeviceState* ds, const void* Q, const void* K, const
   }
   p.decode = 1;
   p.q_rows = p.kv_group * Lq;
-  p.kv_chunk = plan.kv_chunk;
-  p.n_chunks = plan.n_chunks;
+  p.n_chunks = slots;
   p.n_qblocks = 1;
-  p.n_items = static_cast<int>(static_cast<long long>(B) * h_kv * plan.n_chunks);
+  p.n_items = grid;  // one CTA per SM; the kernel splits the key tiles among them
   p.part_o = reinterpret_cast<float*>(ws);
-  p.part_ml = reinterpret_cast<float*>(ws + decode_part_o_bytes(rows, plan.n_chunks, d));
+  p.part_ml = reinterpret_cast<float*>(ws + decode_part_o_bytes(rows, slots, d));
   st = d == 64 ? launch_attn<64, ATTN_SCHEDULE_SPLIT_KEYS>(ds, mq, mk, mv, p, s)
                : launch_attn<128, ATTN_SCHEDULE_SPLIT_KEYS>(ds, mq, mk, mv, p, s);
   if (st != ATTN_OK) return st;
-  const unsigned grid = static_cast<unsigned>((rows + 3) / 4);
+  const unsigned cgrid = static_cast<unsigned>((rows + 3) / 4);
   if (d == 64)
-    gb300::attn_decode_combine_kernel<64><<<grid, 128, 0, s>>>(
-        p.part_o, p.part_ml, plan.n_chunks, rows, static_cast<__nv_bfloat16*>(O), LSE);
+    gb300::attn_decode_combine_kernel<64><<<cgrid, 128, 0, s>>>(
+        p, grid, rows, static_cast<__nv_bfloat16*>(O), LSE);
   else
-    gb300::attn_decode_combine_kernel<128><<<grid, 128, 0, s>>>(
-        p.part_o, p.part_ml, plan.n_chunks, rows, static_cast<__nv_bfloat16*>(O), LSE);
+    gb300::attn_decode_combine_kernel<128><<<cgrid, 128, 0, s>>>(
+        p, grid, rows, static_cast<__nv_bfloat16*>(O), LSE);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -769,10 +757,9 @@ size_t attn_decode_workspace_bytes(int B, int h, int h_kv, int Lq, int Lk, int d
   if (B <= 0 || h <= 0 || h_kv <= 0 || Lq <= 0 || Lk <= 0 || (d != 64 && d != 128)) return 0;
   DeviceState* ds = nullptr;
   if (device_state(&ds, nullptr) != ATTN_OK) return 0;
-  const DecodePlan plan = decode_plan(ds->num_sms, B, h_kv, Lk);
+  const int slots = decode_slots(ds->num_sms, Lk);
   const long long rows = static_cast<long long>(B) * h * Lq;
-  return decode_part_o_bytes(rows, plan.n_chunks, d) +
-         static_cast<size_t>(rows) * plan.n_chunks * 4 * sizeof(float);
+  return decode_part_o_bytes(rows, slots, d) + static_cast<size_t>(rows) * slots * 4 * sizeof(float);
 }
 
 attn_status_t attn_decode(const void* Q, const void* K, const void* V, int B, int h, int h_kv,
