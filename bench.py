@@ -39,6 +39,8 @@ METRIC = "attention fwd TFLOP/s on 1 GB300 and % of roofline (tensor/exp/HBM bou
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # sources whose hash a committed DRAM-traffic figure is tied to, per kernel
+E2E_WINDOWS = 3  # end-to-end timing windows; the median one is reported
+
 KERNEL_SOURCES = {
     "attn_fwd_kernel": ["attn_fwd_kernel.cuh", "ptx.cuh"],
     "gemm_bf16_kernel": ["gemm_kernel.cuh", "ptx.cuh"],
@@ -463,16 +465,22 @@ def ours_arm(args, w):
 
     e2e_step()
     torch.cuda.synchronize(dev)
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    # the host link is shared with other users of the machine and now and then
+    # runs at half rate for a while: time E2E_WINDOWS windows of e2e_steps
+    # steps and report the median window (all of them are listed)
+    e2e_windows = []
+    for _ in range(E2E_WINDOWS):
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e2e_windows.append(max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world))
+    e2e_ms = statistics.median(e2e_windows)
     g.check_device_status(stream)
 
     flops, exps, hbm_bytes = algorithmic_counts(w, kv_lens)
@@ -523,7 +531,8 @@ def ours_arm(args, w):
                                                              if decode else
                                                              hk.numel() * 2 + hv.numel() * 2)),
                 "d2h_bytes_per_step": int(hO.numel() * 2 + hL.numel() * 4),
-                "steps": e2e_steps, "ms_per_step": e2e_ms, "api": e2e_api},
+                "steps": e2e_steps, "ms_per_step": e2e_ms, "windows_ms_per_step": e2e_windows,
+                "api": e2e_api},
         "gpu_launches": (2 if w.kind == "decode" else 1) * args.steps,
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -636,7 +645,8 @@ def layer_arm(args, w):
                              workspace=hws, stream=stream)
 
     e2e_step()
-    e2e_ms = max_over_ranks(timed(e2e_step, e2e_steps), world)
+    e2e_windows = [max_over_ranks(timed(e2e_step, e2e_steps), world) for _ in range(E2E_WINDOWS)]
+    e2e_ms = statistics.median(e2e_windows)
 
     proj, attn = layer_flops(w)
     flops = proj + attn
@@ -683,7 +693,7 @@ def layer_arm(args, w):
                           if flush is not None else "inputs larger than L2, no flush")},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(hx.numel() * 2), "d2h_bytes_per_step": int(hy.numel() * 2),
-                "steps": e2e_steps, "ms_per_step": e2e_ms,
+                "steps": e2e_steps, "ms_per_step": e2e_ms, "windows_ms_per_step": e2e_windows,
                 "api": "mha_layer_fwd_host (copies overlapped with the kernels)"},
         "gpu_launches": 3 * args.steps,
         "roofline": roofline,
