@@ -79,6 +79,7 @@ struct AttnParams {
   int o_v8;                // 1: O and its strides are 32-byte aligned (256-bit stores)
   float* LSE;              // [B,H,Lq] natural-log LSE, or nullptr
   int n_qblocks;           // ceil(Lq / 256)
+  int head_group;          // (b, h) pairs per group of the item order; B * H: one group
   int n_items;             // B * H * n_qblocks
   unsigned int* status;    // device status word
   unsigned long long wait_limit_ns;
@@ -144,16 +145,22 @@ struct AttnItem {
 
 // Item k of this CTA.  Items are ordered heaviest first (query blocks from
 // the end of the sequence, which under the causal mask see the most keys)
-// and dealt to CTAs in a boustrophedon order, which balances the triangular
-// work without any atomics.
+// within each group of heads, and dealt to CTAs in a boustrophedon order,
+// which balances the triangular work without any atomics.
 __device__ __forceinline__ bool attn_get_item(const AttnParams& p, int k, AttnItem& it) {
   const int G = static_cast<int>(gridDim.x);
   const int c = static_cast<int>(blockIdx.x);
   const long long w = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
   if (w >= p.n_items) return false;
-  const int BH = p.B * p.H;
-  const int rank = static_cast<int>(w / BH);
-  const int bh = static_cast<int>(w - static_cast<long long>(rank) * BH);
+  // Items go group by group of head_group (b, h) pairs (it divides B * H),
+  // heaviest first within a group, so that the K/V a group streams can stay
+  // in L2 while its items run.
+  const int HG = p.head_group;
+  const long long per_group = static_cast<long long>(HG) * p.n_qblocks;
+  const int grp = static_cast<int>(w / per_group);
+  const int rem = static_cast<int>(w - grp * per_group);
+  const int rank = rem / HG;
+  const int bh = grp * HG + (rem - rank * HG);
   const int qb = p.n_qblocks - 1 - rank;
   it.b = bh / p.H;
   it.h = bh - it.b * p.H;
