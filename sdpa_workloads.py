@@ -138,6 +138,12 @@ WORKLOADS = {
         AttnWorkload("mha_causal_longctx_b1_h32_l32768_d128", B=1, H=32, Lq=32768, Lk=32768,
                      d_k=128, d_v=128, mask_kind=MASK_CAUSAL, seed=1004,
                      boost_frac=0.05, boost=3.0),
+        # a long-context case whose kernel runs in ~3.4 ms (1.1 GB on the
+        # device) and whose items the attention kernel orders by groups of
+        # heads, as on the 32K workload: for profiles that need many passes
+        AttnWorkload("mha_causal_b2_h32_l16384_d128", B=2, H=32, Lq=16384, Lk=16384,
+                     d_k=128, d_v=128, mask_kind=MASK_CAUSAL, seed=1007,
+                     boost_frac=0.05, boost=3.0),
         LayerWorkload("mha_layer_causal_b8_l2048_dm1024_h16", B=8, L=2048, d_model=1024, H=16,
                       mask_kind=MASK_CAUSAL, seed=1005, w_std=1.0 / 32.0),
         DecodeWorkload("gqa_decode_b8_h32_hkv8_lq1_lk32768_d128", B=8, H=32, H_kv=8, Lq=1,

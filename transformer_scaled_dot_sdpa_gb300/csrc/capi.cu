@@ -164,18 +164,23 @@ attn_status_t launch_attn(DeviceState* ds, const CUtensorMap& mq, const CUtensor
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-// Heads per group of the two-Q-tile item order: the largest divisor of B * H
-// whose K/V (shared by kv_group query heads) fits in L2, provided each group
-// still has at least four waves of items; otherwise one group.  Measured on
-// causal B1 h32 L32768 d128 under sustained load (16.8 MB of K/V per head,
-// 135.5 MB of L2): groups of 8 heads 1401 TFLOP/s, one group 1372, 4 heads
-// 1353; a group size that leaves a partial last group (7) fell to 1240.
+// Heads per group of the two-Q-tile item order.  One group (the plain
+// heaviest-first order) unless the K/V of all heads exceeds three times the
+// L2; then the largest divisor of B * H whose K/V (shared by kv_group query
+// heads) fits in L2, provided each group still has at least four waves of
+// items.  Measured at d = 128, causal, in 135.5 MB of L2:
+//   B1 h32 L32768 (537 MB of K/V): groups of 8 heads 1401 TFLOP/s against
+//     1372 under sustained load (1484 against 1502 in a short run); groups of
+//     7, which leave a partial last group, 1240;
+//   B1 h32 L16384 (268 MB): one group 1438, groups of 16 1320, of 8 1415;
+//   B2 h32 L16384 (537 MB): groups of 16 1425, one group 1410.
 int item_head_group(const DeviceState* ds, int B, int H, int H_kv, int Lk, int d,
                     int n_qblocks) {
   const int BH = B * H;
   const int kv_group = H / H_kv;
   const long long kv_head_bytes = 2ll * Lk * d * 2;  // K and V of one K/V head
   const long long min_items = 4ll * ds->num_sms;
+  if (static_cast<long long>(B) * H_kv * kv_head_bytes <= 3 * ds->l2_bytes) return BH;
   for (int hg = BH; hg >= 1; --hg) {
     if (BH % hg != 0) continue;
     // K/V heads the group's query heads touch (one more when the group does
