@@ -176,6 +176,34 @@ def test_longest_sequence_sampled(cuda_lib):
     compare_attention(O.reshape(-1, d)[flat], Lse.reshape(-1)[flat], Or, Lr, "L = 131072")
 
 
+_INPUT_CACHE = {}
+
+
+def test_head_grouped_order_gqa_padding_sampled(cuda_lib):
+    """A shape whose K/V (537 MB) is over three times the L2, so the kernel
+    orders its items by groups of heads: grouped-query attention (2 query
+    heads per K/V head) with the causal and padding masks together.  A
+    stratified sample of rows of every head (padded rows included) against the
+    oracle."""
+    import torch
+    B, H, H_kv, L, d = 2, 32, 16, 32768, 128
+    if "gqa_grouped" not in _INPUT_CACHE:  # the test runs once per schedule
+        _INPUT_CACHE["gqa_grouped"] = make_attention_inputs(B, H, L, L, d, d, seed=77, H_kv=H_kv)
+    inp = _INPUT_CACHE["gqa_grouped"]
+    kv = np.array([32768, 20000], dtype=np.int32)
+    O, Lse = cuda_lib.attn_fwd(up(inp["q"]), up(inp["k"]), up(inp["v"]),
+                               mask_kind=MASK_CAUSAL | MASK_PADDING,
+                               kv_lens=torch.from_numpy(kv).cuda())
+    cuda_lib.check_device_status()
+    O, Lse = down(O), Lse.cpu().numpy()
+    rows_in_head = sample_rows(L, 12, seed=77)
+    flat = np.concatenate([bh * L + rows_in_head for bh in range(B * H)])
+    Or, Lr = oracle.attention(inp["q"], inp["k"], inp["v"], mask_kind=MASK_CAUSAL | MASK_PADDING,
+                              kv_lens=kv, rows=flat)
+    compare_attention(O.reshape(-1, d)[flat], Lse.reshape(-1)[flat], Or, Lr,
+                      "grouped order, GQA + padding")
+
+
 _ORACLE_CACHE = {}
 
 
