@@ -16,10 +16,11 @@
  *     -- "attention-mechanism" page, sections "公式：为什么要除以 sqrt(d_k)"
  *        (scale is the per-head d_k) and "掩码：因果与 padding".
  *
- *   For each (b, head, query row i), in fp64:
- *     J_i  = { j < Lk }  intersected with { j <= i } if CAUSAL
- *                        intersected with { j <= i + Lk - Lq } if CAUSAL_BR
- *                        intersected with { j < kv_len[b] } if PADDING
+ *   For each (b, head, query row i), in fp64, with n_b the keys of
+ *   sequence b (kv_len[b] if PADDING, else Lk):
+ *     J_i  = { j < n_b }  intersected with { j <= i } if CAUSAL
+ *                         intersected with { j <= p_i } if CAUSAL_BR, where
+ *                         p_i = n_b - Lq + i is the query's own position
  *     s_j  = scale * sum_c Q[i,c] K[j,c]          for j in J_i
  *     m    = max_j s_j                            (max subtraction, the
  *                                                  stable softmax form of the
@@ -29,8 +30,9 @@
  *     A_ij = e_j / l  (0 for j not in J_i)
  *     O[i] = sum_j e_j V[j] / l
  *     LSE[i] = m + log(l)
- *   A padded query row (PADDING and i >= kv_len[b]) or a row whose J_i is
- *   empty has O[i] = 0 and LSE[i] = -inf.
+ *   A padded query row (PADDING without CAUSAL_BR, and i >= kv_len[b]) or a
+ *   row whose J_i is empty (CAUSAL_BR and p_i < 0) has O[i] = 0 and
+ *   LSE[i] = -inf.
  *
  *   Grouped-query attention ("Self-Attention 机制", section
  *   "MHA -> MQA -> GQA -> MLA"): with H query heads and Hkv key/value heads
@@ -38,10 +40,17 @@
  *   K/V head: query head h reads K/V head h / (H/Hkv).  Hkv = H is ordinary
  *   multi-head attention, Hkv = 1 multi-query attention.
  *
- *   CAUSAL_BR is the causal mask aligned to the last key instead of the first
- *   (query i sits at key position i + Lk - Lq), the reading used when Lq
- *   queries continue a sequence whose Lk keys include them; for Lq = Lk it is
- *   the ordinary causal mask.
+ *   CAUSAL_BR is the causal mask aligned to the last key of each sequence
+ *   instead of the first: the Lq queries are the sequence's last Lq tokens,
+ *   so query i sits at position p_i = n_b - Lq + i and, by the look-ahead
+ *   rule ("04. Self-Attention", section 七; "Self-Attention 机制", section
+ *   "Causal Mask": a token never sees a later one), sees the keys j <= p_i.
+ *   This is the reading for Lq new tokens decoded against a cache that
+ *   already holds them (same page, the KV Cache of section
+ *   "MHA -> MQA -> GQA -> MLA"): with per-sequence lengths (PADDING) each
+ *   sequence's new tokens sit at its own end, and new token i never sees new
+ *   token i + 1.  Without PADDING (n_b = Lk), and for Lq = Lk, it is the
+ *   ordinary causal mask shifted by Lk - Lq.
  *
  *   The multi-head layer ("Self-Attention 机制", section "五步计算" and the
  *   shape trace in "维度全程跟踪"; "多模态大模型学习笔记（十四）", section 3.3):
@@ -138,23 +147,26 @@ static void attend_row(const double *q, const double *K, size_t k_stride,
     *lse = m + log(l);
 }
 
-/* Number of keys row i of batch b may attend to (J_i is always a prefix). */
+/*
+ * Number of keys query row i of a sequence may attend to (J_i is always a
+ * prefix).  kv_len is the sequence's own length when PADDING is set.
+ */
 static int valid_keys(int i, int Lq, int Lk, int mask_kind, int kv_len)
 {
-    int n = Lk;
+    const int padding = (mask_kind & OR_MASK_PADDING) != 0;
+    const int n_seq = padding ? kv_len : Lk; /* keys of this sequence */
+    int n = n_seq;
+    if (mask_kind & OR_MASK_CAUSAL_BR) {
+        /* the queries are the sequence's last Lq tokens: row i is at p_i */
+        long long pos = (long long)n_seq - (long long)Lq + (long long)i;
+        if (pos < 0)
+            return 0; /* the query precedes the sequence: no keys, output 0 */
+        return (int)(pos + 1); /* keys 0..p_i; p_i < n_seq because i < Lq */
+    }
+    if (padding && i >= kv_len)
+        return 0; /* padded query row: output 0 */
     if (mask_kind & OR_MASK_CAUSAL)
         n = (i + 1 < n) ? i + 1 : n;
-    if (mask_kind & OR_MASK_CAUSAL_BR) {
-        long long lim = (long long)i + 1 + (long long)Lk - (long long)Lq;
-        if (lim < 0)
-            lim = 0;
-        n = (lim < n) ? (int)lim : n;
-    }
-    if (mask_kind & OR_MASK_PADDING) {
-        if (i >= kv_len)
-            return 0; /* padded query row: output 0 */
-        n = (kv_len < n) ? kv_len : n;
-    }
     return n;
 }
 

@@ -428,6 +428,95 @@ def bottom_right_causal_mask(orc):
         assert np.all(O[:, :, ~live] == 0.0) and np.all(np.isneginf(Lse[:, :, ~live]))
 
 
+@pin
+def bottom_right_causal_with_padding_is_per_sequence(orc):
+    """Bottom-right causal with per-sequence lengths: the Lq queries are the
+    last Lq tokens of sequence b, query i sits at position kv_len_b - Lq + i
+    and sees keys up to and including that position (P-a 七 and P-e Causal
+    Mask: a token never sees a later one).  So the result for sequence b is
+    the bottom-right causal result on its truncated keys K[:kv_len_b], bit
+    for bit, and rows whose position is negative are empty (O = 0,
+    LSE = -inf).  Checked with grouped K/V heads too."""
+    BR = 4
+    rng = np.random.default_rng(191)
+    for (Lq, Lk, H, Hkv) in ((2, 8, 2, 2), (5, 20, 4, 2), (1, 13, 3, 1), (7, 7, 2, 1)):
+        kvl = np.array([Lk, Lk // 2, Lq, max(Lq - 1, 0), 1, 0], dtype=np.int32)
+        B = kvl.shape[0]
+        q = rng.standard_normal((B, H, Lq, 8))
+        k = rng.standard_normal((B, Hkv, Lk, 8))
+        v = rng.standard_normal((B, Hkv, Lk, 6))
+        O, Lse = orc.attention(q, k, v, mask_kind=BR | MASK_PADDING, kv_lens=kvl)
+        for b in range(B):
+            n = int(kvl[b])
+            live = np.arange(Lq) >= Lq - n  # position n - Lq + i >= 0
+            if n > 0:
+                Ob, Lb = orc.attention(q[b:b + 1], k[b:b + 1, :, :n], v[b:b + 1, :, :n],
+                                       mask_kind=BR)
+                assert np.array_equal(O[b:b + 1], Ob) and np.array_equal(Lse[b:b + 1], Lb)
+            assert np.all(O[b][:, ~live] == 0.0) and np.all(np.isneginf(Lse[b][:, ~live]))
+            assert np.all(np.isfinite(Lse[b][:, live]))
+
+
+@pin
+def decode_with_cache_equals_full_causal_self_attention(orc):
+    """The KV-cache identity (P-e, the KV Cache of MHA -> MQA -> GQA -> MLA,
+    with the look-ahead mask of P-a 七): for a sequence of n tokens,
+    causal self-attention over all n and then taking its last Lq rows equals
+    the bottom-right causal attention of those Lq queries against a cache
+    holding the n tokens (padded to Lk with junk past n).  Each new token
+    gives weight exactly 0 to every later new token, and a positive weight
+    to every token up to itself."""
+    BR = 4
+    rng = np.random.default_rng(192)
+    H, dk, dv, Lk = 2, 8, 8, 24
+    for Lq in (2, 4, 16):
+        for n in (Lq, Lq + 3, Lk):
+            qf = rng.standard_normal((1, H, n, dk))
+            kf = rng.standard_normal((1, H, n, dk))
+            vf = rng.standard_normal((1, H, n, dv))
+            Of, Lf = orc.attention(qf, kf, vf, mask_kind=MASK_CAUSAL)
+            kc = rng.standard_normal((1, H, Lk, dk)) * 50.0  # junk past n
+            vc = rng.standard_normal((1, H, Lk, dv)) * 50.0
+            kc[:, :, :n], vc[:, :, :n] = kf, vf
+            kvl = np.array([n], dtype=np.int32)
+            O, Lse, A = orc.attention(qf[:, :, n - Lq:], kc, vc, mask_kind=BR | MASK_PADDING,
+                                      kv_lens=kvl, want_weights=True)
+            assert np.array_equal(O, Of[:, :, n - Lq:])
+            assert np.array_equal(Lse, Lf[:, :, n - Lq:])
+            for i in range(Lq):
+                pos = n - Lq + i
+                assert np.all(A[0, :, i, pos + 1:] == 0.0)
+                assert np.all(A[0, :, i, :pos + 1] > 0.0)
+
+
+@pin
+def bottom_right_causal_with_padding_matches_torch(orc):
+    """PyTorch SDPA in float64 with the boolean mask written out per
+    sequence: keep (i, j) iff j <= kv_len_b - Lq + i (which also keeps
+    j < kv_len_b).  Rows with no key kept are empty."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    BR = 4
+    Lq, Lk = 6, 17
+    kvl = np.array([17, 9, 6, 3], dtype=np.int32)
+    rng = np.random.default_rng(193)
+    q = rng.standard_normal((4, 2, Lq, 8))
+    k = rng.standard_normal((4, 2, Lk, 8))
+    v = rng.standard_normal((4, 2, Lk, 8))
+    O, Lse = orc.attention(q, k, v, mask_kind=BR | MASK_PADDING, kv_lens=kvl)
+    for b in range(4):
+        keep = (np.arange(Lk)[None, :] <= (kvl[b] - Lq + np.arange(Lq))[:, None])
+        live = keep.any(axis=1)
+        tO = F.scaled_dot_product_attention(
+            torch.from_numpy(q[b:b + 1]), torch.from_numpy(k[b:b + 1]),
+            torch.from_numpy(v[b:b + 1]), attn_mask=torch.from_numpy(keep)).numpy()
+        np.testing.assert_allclose(O[b:b + 1][:, :, live], tO[:, :, live], atol=1e-12)
+        ls = torch.logsumexp(torch.from_numpy(q[b] @ k[b].transpose(0, 2, 1) / math.sqrt(8))
+                             .masked_fill(~torch.from_numpy(keep), -math.inf), dim=-1).numpy()
+        np.testing.assert_allclose(Lse[b][:, live], ls[:, live], atol=1e-12)
+        assert np.all(O[b][:, ~live] == 0.0) and np.all(np.isneginf(Lse[b][:, ~live]))
+
+
 # ---------------------------------------------------------------------------
 # the five-step layer
 # ---------------------------------------------------------------------------
@@ -556,7 +645,8 @@ MUTANTS = [
      "J.scale = scale > 0.0 ? scale : 1.0 / (double)dk;"),
     ("no_scale", "s[j] = scale * dot;", "s[j] = dot;"),
     ("causal_off_by_one", "n = (i + 1 < n) ? i + 1 : n;", "n = (i < n) ? i : n;"),
-    ("padding_keys_unmasked", "n = (kv_len < n) ? kv_len : n;", ";"),
+    ("padding_keys_unmasked", "const int n_seq = padding ? kv_len : Lk;",
+     "const int n_seq = Lk;"),
     ("padded_queries_not_zeroed", "return 0; /* padded query row: output 0 */", ";"),
     ("no_normalisation", "o[c] /= l;", ";"),
     ("lse_without_max", "*lse = m + log(l);", "*lse = log(l);"),
@@ -575,8 +665,19 @@ MUTANTS = [
      "const double *Kh = J->Kp + (size_t)slot * J->L * dm;"),
     ("gqa_heads_not_grouped", "kvbh = (int64_t)b * J->Hkv + (int)(bh % J->H) / (J->H / J->Hkv);",
      "kvbh = (int64_t)b * J->Hkv + (int)(bh % J->H) % J->Hkv;"),
-    ("causal_br_offset_sign", "long long lim = (long long)i + 1 + (long long)Lk - (long long)Lq;",
-     "long long lim = (long long)i + 1 + (long long)Lq - (long long)Lk;"),
+    ("causal_br_offset_sign", "long long pos = (long long)n_seq - (long long)Lq + (long long)i;",
+     "long long pos = (long long)Lq - (long long)n_seq + (long long)i;"),
+    # the reading this oracle replaced: the offset Lk - Lq for every sequence,
+    # with the first kv_len query rows live, so a new token saw later ones
+    ("causal_br_offset_from_cache_size",
+     "long long pos = (long long)n_seq - (long long)Lq + (long long)i;\n"
+     "        if (pos < 0)\n"
+     "            return 0; /* the query precedes the sequence: no keys, output 0 */\n"
+     "        return (int)(pos + 1);",
+     "long long pos = (long long)Lk - (long long)Lq + (long long)i;\n"
+     "        if (pos < 0 || (padding && i >= kv_len))\n"
+     "            return 0;\n"
+     "        return (pos + 1 < n) ? (int)(pos + 1) : n;"),
     ("layer_wo_transposed", "J.Wo_d[(size_t)c * dm + n] = widen_bf16(Wo[(size_t)c * dm + n]);",
      "J.Wo_d[(size_t)n * dm + c] = widen_bf16(Wo[(size_t)c * dm + n]);"),
 ]
