@@ -61,11 +61,16 @@ typedef enum {
  * causal flags are exclusive.
  *   ATTN_MASK_CAUSAL: key j is hidden from query i when j > i (the look-ahead
  *     mask, aligned to the first key).
- *   ATTN_MASK_CAUSAL_BOTTOM_RIGHT: key j is hidden from query i when
- *     j > i + (Lk - Lq): the same mask aligned to the last key, for Lq queries
- *     that continue a sequence of Lk keys which includes them (e.g. decoding
- *     against a KV cache).  Equal to ATTN_MASK_CAUSAL when Lq == Lk; a query
- *     with no visible key (Lq > Lk) gets O = 0, LSE = -inf.
+ *   ATTN_MASK_CAUSAL_BOTTOM_RIGHT: the same look-ahead mask aligned to the
+ *     last key of each sequence, for Lq queries that are the last Lq tokens
+ *     of a sequence whose keys include them (decoding against a KV cache,
+ *     "Self-Attention 机制", sections "Causal Mask" and "MHA -> MQA -> GQA ->
+ *     MLA").  Sequence b holds n_b keys: kv_lens[b] with ATTN_MASK_PADDING,
+ *     else Lk.  Query i sits at position p_i = n_b - Lq + i and sees the keys
+ *     j <= p_i, so a new token never sees a later new token.  A query with
+ *     p_i < 0 sees no key and gets O = 0, LSE = -inf; with this mask no query
+ *     row is padding by its index alone.  Without padding it is the shift by
+ *     Lk - Lq, equal to ATTN_MASK_CAUSAL when Lq == Lk.
  */
 enum {
   ATTN_MASK_NONE = 0,
@@ -83,7 +88,9 @@ enum {
  *                               log-sum-exp of the row's scaled, masked scores
  *   kv_lens int32 [B] device array, required iff mask_kind has the PADDING
  *     bit: sequence b's valid length.  Keys j >= kv_lens[b] are masked; query
- *     rows i >= kv_lens[b] are padding and get O = 0, LSE = -inf.
+ *     rows i >= kv_lens[b] are padding and get O = 0, LSE = -inf (except
+ *     with ATTN_MASK_CAUSAL_BOTTOM_RIGHT, whose queries end at the sequence's
+ *     end: see above).
  *   mask_kind: ATTN_MASK_* flags (see above).
  *   scale: multiplier of Q K^T; scale <= 0 selects 1 / sqrt(d_k).
  *   A row with no visible key (kv_lens[b] == 0, or Lk == 0) gets O = 0 and
@@ -204,7 +211,10 @@ size_t attn_decode_workspace_bytes(int B, int h, int h_kv, int Lq, int Lk, int d
  *   K_cache, V_cache  device bf16 [B, h_kv, Lk, d], 16-byte aligned; the
  *            call writes row kv_len_b - Lq + i of (b, K/V head) with new row
  *            i (rows whose position would be negative are dropped) and
- *            reads the cache as attn_decode does.
+ *            reads the cache as attn_decode does.  That row is the position
+ *            ATTN_MASK_CAUSAL_BOTTOM_RIGHT gives query i, so each new token
+ *            sees the cache up to and including its own key, and no later
+ *            new token.
  *   kv_lens  host int32 [B] (required with ATTN_MASK_PADDING): valid keys
  *            of each sequence after the new ones are appended, clamped to
  *            [0, Lk].  Without padding every sequence holds Lk keys and the

@@ -71,6 +71,11 @@ struct AttnParams {
   int kv_group;            // query heads per K/V head (grouped-query attention)
   int causal_offset;       // causal: query i sees keys j <= i + causal_offset
   int mask_kind;           // bit 0 causal, bit 1 padding
+  // 1: bottom-right causal with padding.  The queries are the last Lq tokens
+  // of each sequence: sequence b's offset is kv_len_b - Lq (causal_offset is
+  // unused) and no query row is padding by its index; rows before the
+  // sequence's first token see no key.
+  int offset_per_seq;
   int packed;              // 0: Q/K/V maps over [B,H,L,d]; 1: over [B,L,3,H,d]
   const int32_t* kv_lens;  // [B] valid lengths (padding) or nullptr
   float scale_log2;        // softmax scale * log2(e)
@@ -95,6 +100,21 @@ struct AttnParams {
   float* part_o;           // [B*H*Lq][n_chunks][D]: w_0 O_0 + w_1 O_1 of the item
   float* part_ml;          // [B*H*Lq][n_chunks][4]: m (log2 units), l, lb, 0
 };
+
+// Causal offset of a sequence with kv_len valid keys: its query i sees the
+// keys j <= i + offset ("04. Self-Attention", section 七: no token sees a
+// later one).  Top-left: 0; bottom-right: Lk - Lq, or kv_len - Lq when each
+// sequence has its own length, so that its queries sit at its own end.
+__device__ __forceinline__ int attn_causal_offset(const AttnParams& p, int kv_len) {
+  return p.offset_per_seq ? kv_len - p.Lq : p.causal_offset;
+}
+
+// A padded query row (O = 0, LSE = -inf): with the padding mask, rows at or
+// past the sequence's length -- except under the bottom-right causal mask,
+// whose queries end at the sequence's end.
+__device__ __forceinline__ bool attn_padded_query(const AttnParams& p, int r, int kv_len) {
+  return (p.mask_kind & ATTN_MASK_PADDING_BIT) && !p.offset_per_seq && r >= kv_len;
+}
 
 template <int D>
 struct AttnLayout {
@@ -141,6 +161,7 @@ struct AttnItem {
   int nkv_max;
   int kv_len;             // valid keys of this sequence (Lk without padding)
   int kv_len_raw;         // as given (for range reporting)
+  int coff;               // causal offset of this sequence (attn_causal_offset)
 };
 
 // Item k of this CTA.  Items are ordered heaviest first (query blocks from
@@ -180,18 +201,19 @@ __device__ __forceinline__ bool attn_get_item(const AttnParams& p, int k, AttnIt
     kv_len = raw < 0 ? 0 : (raw > p.Lk ? p.Lk : raw);
   }
   it.kv_len = kv_len;
+  it.coff = attn_causal_offset(p, kv_len);
   it.nkv_max = 0;
 #pragma unroll
   for (int t = 0; t < ATTN_QTILES; ++t) {
     const int r0 = qb * ATTN_ROWS_PER_ITEM + t * ATTN_BLOCK_M;
     it.row0[t] = r0;
     int n = 0;
-    const bool all_padded = (p.mask_kind & ATTN_MASK_PADDING_BIT) && r0 >= kv_len;
+    const bool all_padded = attn_padded_query(p, r0, kv_len);
     if (r0 < p.Lq && !all_padded) {
       int lim = kv_len;
       if (p.mask_kind & ATTN_MASK_CAUSAL_BIT) {
         const int last = min(r0 + ATTN_BLOCK_M - 1, p.Lq - 1);
-        lim = min(lim, max(last + 1 + p.causal_offset, 0));
+        lim = min(lim, max(last + 1 + it.coff, 0));
       }
       n = (lim + ATTN_BLOCK_N - 1) / ATTN_BLOCK_N;
     }
@@ -454,7 +476,6 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
   const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(t) * L::O_STRIDE + lane_base;
   const float c = p.scale_log2;
   const bool causal = (p.mask_kind & ATTN_MASK_CAUSAL_BIT) != 0;
-  const bool padding = (p.mask_kind & ATTN_MASK_PADDING_BIT) != 0;
   uint32_t s_cnt = 0, o_cnt = 0;  // completions seen of S_FULL[t], O_DONE[t]
   bool ok = true;
   AttnItem it;
@@ -464,8 +485,8 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
     if (row0 >= p.Lq) continue;  // tile wholly past the end of the sequence
     const int r = row0 + rloc;
     int limit = it.kv_len;  // this row attends to keys [0, limit)
-    if (causal) limit = min(limit, max(r + 1 + p.causal_offset, 0));
-    const bool padded_row = padding && r >= it.kv_len;
+    if (causal) limit = min(limit, max(r + 1 + it.coff, 0));
+    const bool padded_row = attn_padded_query(p, r, it.kv_len);
     float m = -INFINITY, l = 0.f, lb = 0.f;
     for (int j = 0; j < nkv; ++j) {
       ok = mbar_wait(&bars[L::B_S_FULL + t], s_cnt & 1u, ctl);

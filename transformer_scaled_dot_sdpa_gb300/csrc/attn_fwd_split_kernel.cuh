@@ -42,6 +42,7 @@ constexpr int SPLIT_ROWS = 128;  // query rows per work item
 
 struct SplitItem {
   int b, h, kvh, row0, nkv, kv_len, kv_len_raw;
+  int coff;   // causal offset of the sequence (attn_causal_offset)
   int k0;     // first key of the item's key range
   int chunk;  // decode: slot of the item's partial result among its pair's
   int qrow;   // decode: flat index of the first packed Q row
@@ -61,7 +62,8 @@ __device__ __forceinline__ int decode_seq_tiles(const AttnParams& p, int b) {
     len = raw < 0 ? 0 : (raw > p.Lk ? p.Lk : raw);
   }
   // keys the last query row may see bound those of every row of the pair
-  if (p.mask_kind & ATTN_MASK_CAUSAL_BIT) len = min(len, max(p.Lq + p.causal_offset, 0));
+  if (p.mask_kind & ATTN_MASK_CAUSAL_BIT)
+    len = min(len, max(p.Lq + attn_causal_offset(p, len), 0));
   return (len + ATTN_BLOCK_N - 1) / ATTN_BLOCK_N;
 }
 
@@ -124,6 +126,7 @@ __device__ __forceinline__ bool split_get_item(const AttnParams& p, int k, Split
           kv_len = raw < 0 ? 0 : (raw > p.Lk ? p.Lk : raw);
         }
         it.kv_len = kv_len;
+        it.coff = attn_causal_offset(p, kv_len);
         it.row0 = 0;
         it.k0 = t0 * ATTN_BLOCK_N;
         it.nkv = static_cast<int>(end - x);
@@ -165,14 +168,15 @@ __device__ __forceinline__ bool split_get_item(const AttnParams& p, int k, Split
     kv_len = raw < 0 ? 0 : (raw > p.Lk ? p.Lk : raw);
   }
   it.kv_len = kv_len;
+  it.coff = attn_causal_offset(p, kv_len);
   it.row0 = qt * SPLIT_ROWS;
   int n = 0;
-  const bool all_padded = (p.mask_kind & ATTN_MASK_PADDING_BIT) && it.row0 >= kv_len;
+  const bool all_padded = attn_padded_query(p, it.row0, kv_len);
   if (it.row0 < p.Lq && !all_padded) {
     int lim = kv_len;
     if (p.mask_kind & ATTN_MASK_CAUSAL_BIT) {
       const int last = min(it.row0 + SPLIT_ROWS - 1, p.Lq - 1);
-      lim = min(lim, max(last + 1 + p.causal_offset, 0));
+      lim = min(lim, max(last + 1 + it.coff, 0));
     }
     n = (lim + ATTN_BLOCK_N - 1) / ATTN_BLOCK_N;
   }
@@ -416,7 +420,6 @@ __device__ __forceinline__ void split_softmax_role(const int g, const AttnParams
   uint64_t* xbar = &bars[L::B_XCHG + q];
   const float c = p.scale_log2;
   const bool causal = (p.mask_kind & ATTN_MASK_CAUSAL_BIT) != 0;
-  const bool padding = (p.mask_kind & ATTN_MASK_PADDING_BIT) != 0;
   uint32_t t0 = 0;     // running index of the item's first tile
   uint32_t x_cnt = 0;  // exchanges with the other group
   bool ok = true;
@@ -429,8 +432,8 @@ __device__ __forceinline__ void split_softmax_role(const int g, const AttnParams
     const bool live_row = p.decode ? rloc < p.q_rows : r < p.Lq;
     const int nkv = it.nkv;
     int limit = it.kv_len;  // this row attends to keys [0, limit)
-    if (causal) limit = min(limit, max(r + 1 + p.causal_offset, 0));
-    const bool padded_row = padding && r >= it.kv_len;
+    if (causal) limit = min(limit, max(r + 1 + it.coff, 0));
+    const bool padded_row = attn_padded_query(p, r, it.kv_len);
     float m = -INFINITY, l = 0.f, lb = 0.f;
     int cnt = 0;  // tiles of this item taken by this group
     // this group's first tile of the item

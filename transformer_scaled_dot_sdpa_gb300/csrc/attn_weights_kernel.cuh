@@ -19,6 +19,7 @@ struct WeightsParams {
   int B, H, Hkv, Lq, Lk, d;
   int mask_kind;           // bit 0 causal, bit 1 padding
   int causal_offset;       // causal: query i sees keys j <= i + causal_offset
+  int offset_per_seq;      // 1: bottom-right causal with padding, offset kv_len_b - Lq
   const int32_t* kv_lens;
   float scale;
 };
@@ -52,13 +53,17 @@ __global__ void attn_weights_kernel(const WeightsParams p) {
   const int i = i0 + static_cast<int>(threadIdx.y);
   const int j = j0 + static_cast<int>(threadIdx.x);
   if (i >= p.Lq || j >= p.Lk) return;
+  // the same visible-key rule as the forward kernels (attn_causal_offset,
+  // attn_padded_query): keys [0, limit) of row i
   int limit = p.Lk;
+  int coff = p.causal_offset;
   if (p.mask_kind & 2) {
     int kl = p.kv_lens[b];
     kl = kl < 0 ? 0 : (kl > p.Lk ? p.Lk : kl);
-    limit = (i >= kl) ? 0 : kl;
+    limit = (i >= kl && !p.offset_per_seq) ? 0 : kl;
+    if (p.offset_per_seq) coff = kl - p.Lq;
   }
-  if (p.mask_kind & 1) limit = min(limit, max(i + 1 + p.causal_offset, 0));
+  if (p.mask_kind & 1) limit = min(limit, max(i + 1 + coff, 0));
   const float lse = p.LSE[static_cast<long long>(bh) * p.Lq + i];
   float a = 0.f;
   if (j < limit && lse > -INFINITY) {

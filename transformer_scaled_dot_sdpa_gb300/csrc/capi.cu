@@ -147,17 +147,21 @@ attn_status_t launch_attn(DeviceState* ds, const CUtensorMap& mq, const CUtensor
       split ? gb300::attn_fwd_split_kernel<D> : gb300::attn_fwd_kernel<D>;
   if (!ds->attn_attr[attr_idx].load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
-    // The kernels hand registers between warpgroups (setmaxnreg); the split
-    // adds up to exactly ATTN_THREADS x ATTN_REGS_AT_LAUNCH, so a build with a
-    // different launch register count could wait forever: refuse it.
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (fa.numRegs != gb300::ATTN_REGS_AT_LAUNCH || fa.maxThreadsPerBlock < gb300::ATTN_THREADS)
-      return ATTN_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return ATTN_ERR_CUDA;
-    ds->attn_attr[attr_idx].store(true, std::memory_order_release);
+    // re-checked under the lock: of threads racing here, the first does the
+    // set-up and the others find it done
+    if (!ds->attn_attr[attr_idx].load(std::memory_order_relaxed)) {
+      // The kernels hand registers between warpgroups (setmaxnreg); the split
+      // adds up to exactly ATTN_THREADS x ATTN_REGS_AT_LAUNCH, so a build with
+      // a different launch register count could wait forever: refuse it.
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return ATTN_ERR_CUDA;
+      if (fa.numRegs != gb300::ATTN_REGS_AT_LAUNCH || fa.maxThreadsPerBlock < gb300::ATTN_THREADS)
+        return ATTN_ERR_UNSUPPORTED;
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess)
+        return ATTN_ERR_CUDA;
+      ds->attn_attr[attr_idx].store(true, std::memory_order_release);
+    }
   }
   const int grid = p.n_items < ds->num_sms ? p.n_items : ds->num_sms;
   kernel<<<grid, gb300::ATTN_THREADS, smem, stream>>>(mq, mk, mv, p);
@@ -192,6 +196,14 @@ int item_head_group(const DeviceState* ds, int B, int H, int H_kv, int Lk, int d
   return BH;
 }
 
+// Bottom-right causal with per-sequence lengths: the queries are the last Lq
+// tokens of each sequence, so each sequence has its own causal offset
+// kv_len_b - Lq ("04. Self-Attention", section 七: a new token never sees a
+// later one).
+int bottom_right_per_sequence(int mask_kind) {
+  return (mask_kind & ATTN_MASK_CAUSAL_BOTTOM_RIGHT) && (mask_kind & ATTN_MASK_PADDING) ? 1 : 0;
+}
+
 // Shared by attn_fwd and the layer: launch attention with prepared maps.
 attn_status_t run_attention(DeviceState* ds, const CUtensorMap& mq, const CUtensorMap& mk,
                             const CUtensorMap& mv, int packed, int B, int H, int H_kv, int Lq,
@@ -207,6 +219,7 @@ attn_status_t run_attention(DeviceState* ds, const CUtensorMap& mq, const CUtens
   p.kv_group = H / H_kv;
   // both causal alignments are one bit in the kernel plus an offset
   p.causal_offset = (mask_kind & ATTN_MASK_CAUSAL_BOTTOM_RIGHT) ? (Lk - Lq) : 0;
+  p.offset_per_seq = bottom_right_per_sequence(mask_kind);
   p.mask_kind = (mask_kind & ATTN_MASK_PADDING) |
                 ((mask_kind & (ATTN_MASK_CAUSAL | ATTN_MASK_CAUSAL_BOTTOM_RIGHT)) ? 1 : 0);
   p.packed = packed;
@@ -271,22 +284,27 @@ attn_status_t run_gemm(DeviceState* ds, const void* A, const void* Bm, void* C, 
   if ((st = map_2d(&mc, C, M, N, 64, 32)) != ATTN_OK) return st;  // epilogue store boxes
   if (!ds->gemm_attr.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (cudaFuncSetAttribute(gb300::gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gb300::GemmLayout::SMEM_BYTES) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-    // The kernel is persistent: launch only as many pairs as can be resident
-    // together (a TPC with one SM enabled cannot host a pair).
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(static_cast<unsigned>(ds->num_sms & ~1), 1, 1);
-    cfg.blockDim = dim3(gb300::GEMM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = gb300::GemmLayout::SMEM_BYTES;  // cluster size: the kernel's own (2)
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gb300::gemm_bf16_kernel, &cfg) != cudaSuccess ||
-        clusters < 1)
-      return ATTN_ERR_CUDA;
-    ds->gemm_pairs = clusters;
-    ds->gemm_attr.store(true, std::memory_order_release);
+    // re-checked under the lock, as in launch_attn
+    if (!ds->gemm_attr.load(std::memory_order_relaxed)) {
+      if (cudaFuncSetAttribute(gb300::gemm_bf16_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               gb300::GemmLayout::SMEM_BYTES) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+      // The kernel is persistent: launch only as many pairs as can be resident
+      // together (a TPC with one SM enabled cannot host a pair).
+      cudaLaunchConfig_t cfg;
+      std::memset(&cfg, 0, sizeof cfg);
+      cfg.gridDim = dim3(static_cast<unsigned>(ds->num_sms & ~1), 1, 1);
+      cfg.blockDim = dim3(gb300::GEMM_THREADS, 1, 1);
+      cfg.dynamicSmemBytes = gb300::GemmLayout::SMEM_BYTES;  // cluster size: the kernel's (2)
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, gb300::gemm_bf16_kernel, &cfg) !=
+              cudaSuccess ||
+          clusters < 1)
+        return ATTN_ERR_CUDA;
+      ds->gemm_pairs = clusters;
+      ds->gemm_attr.store(true, std::memory_order_release);
+    }
   }
   gb300::GemmParams p;
   std::memset(&p, 0, sizeof p);
@@ -672,6 +690,14 @@ size_t decode_part_o_bytes(long long rows, int n_chunks, int d) {
   return (static_cast<size_t>(rows) * n_chunks * d * 4 + 255) / 256 * 256;
 }
 
+// attn_decode's scratch on a device with num_sms SMs: the partial O of every
+// slot, then its (m, l, lb, 0)
+size_t decode_workspace_bytes(int num_sms, int B, int h, int Lq, int Lk, int d) {
+  const int slots = decode_slots(num_sms, Lk);
+  const long long rows = static_cast<long long>(B) * h * Lq;
+  return decode_part_o_bytes(rows, slots, d) + static_cast<size_t>(rows) * slots * 4 * sizeof(float);
+}
+
 // Argument checks shared by attn_decode and attn_decode_host (no CUDA call).
 attn_status_t check_decode_shape(int B, int h, int h_kv, int Lq, int Lk, int d, int mask_kind,
                                  float scale) {
@@ -752,6 +778,7 @@ attn_status_t decode_device(DeviceState* ds, const void* Q, const void* K, const
   p.Lk = Lk;
   p.kv_group = h / h_kv;
   p.causal_offset = (mask_kind & ATTN_MASK_CAUSAL_BOTTOM_RIGHT) ? (Lk - Lq) : 0;
+  p.offset_per_seq = bottom_right_per_sequence(mask_kind);
   p.mask_kind = (mask_kind & ATTN_MASK_PADDING) |
                 ((mask_kind & (ATTN_MASK_CAUSAL | ATTN_MASK_CAUSAL_BOTTOM_RIGHT)) ? 1 : 0);
   p.kv_lens = kv_lens;
@@ -791,9 +818,7 @@ size_t attn_decode_workspace_bytes(int B, int h, int h_kv, int Lq, int Lk, int d
   if (B <= 0 || h <= 0 || h_kv <= 0 || Lq <= 0 || Lk <= 0 || (d != 64 && d != 128)) return 0;
   DeviceState* ds = nullptr;
   if (device_state(&ds, nullptr) != ATTN_OK) return 0;
-  const int slots = decode_slots(ds->num_sms, Lk);
-  const long long rows = static_cast<long long>(B) * h * Lq;
-  return decode_part_o_bytes(rows, slots, d) + static_cast<size_t>(rows) * slots * 4 * sizeof(float);
+  return decode_workspace_bytes(ds->num_sms, B, h, Lq, Lk, d);
 }
 
 attn_status_t attn_decode(const void* Q, const void* K, const void* V, int B, int h, int h_kv,
@@ -835,7 +860,8 @@ attn_status_t attn_decode_host(const void* Q, const void* K_new, const void* V_n
                                int mask_kind, const int32_t* kv_lens, float scale, void* O,
                                float* LSE, void* workspace, size_t workspace_bytes,
                                void* stream) {
-  // ---- host-side validation (no CUDA call before this point) ----
+  // ---- host-side validation: the arguments alone, then the device's SM
+  // count (device_state, the first CUDA call) for the workspace size ----
   attn_status_t st = check_decode_shape(B, h, h_kv, Lq, Lk, d, mask_kind, scale);
   if (st != ATTN_OK) return st;
   if (B == 0 || h == 0 || Lq == 0) return ATTN_OK;
@@ -847,7 +873,8 @@ attn_status_t attn_decode_host(const void* Q, const void* K_new, const void* V_n
     return ATTN_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds, nullptr)) != ATTN_OK) return st;
-  if (workspace_bytes < attn_decode_host_workspace_bytes(B, h, h_kv, Lq, Lk, d))
+  if (workspace_bytes < decode_host_layout(B, h, h_kv, Lq, d).total +
+                            align256(decode_workspace_bytes(ds->num_sms, B, h, Lq, Lk, d)))
     return ATTN_ERR_INVALID_ARG;
 
   const DecodeHostLayout lay = decode_host_layout(B, h, h_kv, Lq, d);
@@ -921,6 +948,7 @@ attn_status_t attn_weights(const void* Q, const void* K, const float* LSE, int B
   p.mask_kind = (mask_kind & ATTN_MASK_PADDING) |
                 ((mask_kind & (ATTN_MASK_CAUSAL | ATTN_MASK_CAUSAL_BOTTOM_RIGHT)) ? 1 : 0);
   p.causal_offset = (mask_kind & ATTN_MASK_CAUSAL_BOTTOM_RIGHT) ? (Lk - Lq) : 0;
+  p.offset_per_seq = bottom_right_per_sequence(mask_kind);
   p.kv_lens = kv_lens;
   p.scale = scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
   const dim3 grid((Lk + gb300::WEIGHTS_TJ - 1) / gb300::WEIGHTS_TJ,
