@@ -94,14 +94,16 @@ def attention_kernel_name(B, H, Lq, d):
 
 def visible_keys(w, i, kv_len):
     """Keys query row i of a sequence with kv_len valid keys attends to (0 for
-    a padded row), under the workload's mask."""
-    n = w.Lk
+    a padded row), under the workload's mask: the count the FLOPs and exps of
+    a decode step are made of.  Under the bottom-right causal mask the queries
+    are the sequence's last Lq tokens (query i at position n - Lq + i)."""
+    n = kv_len if w.mask_kind & MASK_PADDING else w.Lk
+    if w.mask_kind & MASK_CAUSAL_BOTTOM_RIGHT:
+        return max(n - w.Lq + i + 1, 0)
+    if w.mask_kind & MASK_PADDING and i >= kv_len:
+        return 0
     if w.mask_kind & MASK_CAUSAL:
         n = min(n, i + 1)
-    if w.mask_kind & MASK_CAUSAL_BOTTOM_RIGHT:
-        n = min(n, max(i + 1 + w.Lk - w.Lq, 0))
-    if w.mask_kind & MASK_PADDING:
-        n = 0 if i >= kv_len else min(n, kv_len)
     return n
 
 
@@ -141,7 +143,8 @@ def measure_ex2_rate(g, dev, stream):
 
 
 def algorithmic_counts(w, kv_lens):
-    """FLOPs, exponentials and HBM bytes of one pass (definitions in the design doc)."""
+    """FLOPs, exponentials and HBM bytes of one pass: 4*d FLOPs and one exp per
+    unmasked (query, key) pair; Q, K, V read once and O, LSE written once."""
     if w.kind == "decode":
         # 4*d FLOPs and one exp per visible (row, key) pair; the cache's valid
         # K/V rows read once per K/V head, Q read and O, LSE written once
@@ -361,9 +364,265 @@ def workload_config(w, world, flushed=False):
 
 
 # ---------------------------------------------------------------------------
+# kernel timing and roofline of one workload
+# ---------------------------------------------------------------------------
+def attention_roofline(w, kv_lens, ms, ex2, kernel):
+    """The roofline of one launch: the slowest of tensor FLOPs at the measured
+    bf16 peak, exps at the measured exp2 rate and bytes at the measured HBM
+    bandwidth is the bound; `achieved` and `peak` are in that bound's unit."""
+    flops, exps, hbm_bytes = algorithmic_counts(w, kv_lens)
+    peaks, peak_src = load_peaks()
+    sec = ms * 1e-3
+    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+    t_exp = exps / ex2["exp_per_s"]
+    t_hbm = hbm_bytes / (peaks["hbm_gbs"] * 1e9)
+    bound = max((t_tensor, "tensor"), (t_hbm, "hbm"), (t_exp, "exp"))[1]
+    if bound == "tensor":
+        achieved, peak, unit = flops / sec / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        src = "%s (bf16 dense burst)" % peak_src
+    elif bound == "exp":
+        achieved, peak, unit = exps / sec / 1e12, ex2["exp_per_s"] / 1e12, "Texp/s"
+        src = "measured in this run (attn_probe_ex2)"
+    else:
+        achieved, peak, unit = hbm_bytes / sec / 1e9, peaks["hbm_gbs"], "GB/s"
+        src = "%s (copy bandwidth)" % peak_src
+    roof_ms = 1e3 * max(t_tensor, t_exp, t_hbm)
+    return {
+        "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+        "frac": achieved / peak, "peak_source": src, "kernel": kernel,
+        "traffic": profiled_traffic(w.name, kernel),
+        "tensor_tflops": flops / sec / 1e12,
+        "tensor_frac": flops / sec / 1e12 / peaks["bf16_tflops"],
+        "hbm_gbs": hbm_bytes / sec / 1e9,
+        "hbm_frac": hbm_bytes / sec / 1e9 / peaks["hbm_gbs"],
+        "algorithmic": {"flops": flops, "exps": exps, "hbm_bytes": hbm_bytes},
+        "roofline_time_ms": roof_ms, "frac_of_roofline_time": roof_ms / ms,
+        "exp_bound_fraction": t_exp / max(t_tensor, t_hbm),
+        "exp_rate": {"exp_per_s": ex2["exp_per_s"], "exp_per_clk_per_sm": ex2["exp_per_clk_per_sm"],
+                     "sm_mhz": ex2["sm_mhz"], "source": "measured (attn_probe_ex2)"},
+    }
+
+
+def attention_kernel_name_for(w):
+    if w.kind == "decode":
+        return "attn_fwd_split_kernel<%d> (decode mode)" % w.d_k
+    return attention_kernel_name(w.B, w.H, w.Lq, w.d_k)
+
+
+class AttentionRun:
+    """A workload's inputs resident on the device and its timed kernel calls:
+    warm-up, then `steps` calls between CUDA events on the launching stream
+    with nvidia-smi clocks sampled meanwhile (L2 flushed before each call when
+    the inputs fit in it, and also timed warm)."""
+
+    def __init__(self, g, w, dev, stream, rank=0):
+        import torch
+        self.g, self.w, self.dev, self.stream = g, w, dev, stream
+        self.inp = make_workload_inputs(replica_workload(w, rank))
+        self.kv_lens = self.inp["kv_lens"]
+
+        def pinned(bits):
+            t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+            return t.pin_memory()
+        self.hq, self.hk, self.hv = pinned(self.inp["q"]), pinned(self.inp["k"]), pinned(self.inp["v"])
+        self.q, self.k, self.v = self.hq.to(dev), self.hk.to(dev), self.hv.to(dev)
+        self.kvt = torch.from_numpy(self.kv_lens).to(dev) if self.kv_lens is not None else None
+        self.O = torch.empty((w.B, w.H, w.Lq, w.d_v), dtype=torch.bfloat16, device=dev)
+        self.LSE = torch.empty((w.B, w.H, w.Lq), dtype=torch.float32, device=dev)
+        self.decode = w.kind == "decode"
+        if self.decode:
+            self.ws = torch.empty(g.attn_decode_workspace_bytes(w.B, w.H, w.H_kv, w.Lq, w.Lk, w.d_k),
+                                  dtype=torch.uint8, device=dev)
+
+    def step(self):
+        w, g = self.w, self.g
+        if self.decode:
+            g.attn_decode(self.q, self.k, self.v, mask_kind=w.mask_kind, kv_lens=self.kvt,
+                          scale=w.scale, out=self.O, lse=self.LSE, workspace=self.ws,
+                          stream=self.stream)
+        else:
+            g.attn_fwd(self.q, self.k, self.v, mask_kind=w.mask_kind, kv_lens=self.kvt,
+                       scale=w.scale, out=self.O, lse=self.LSE, stream=self.stream)
+
+    def launches_per_step(self):
+        return 2 if self.decode else 1
+
+    def time(self, steps, warmup, world=1, clock_index=0):
+        import torch
+        for _ in range(warmup):
+            self.step()
+        self.g.check_device_status(self.stream)
+        flush = l2_flush_buffer(attn_input_bytes(self.w), self.dev)
+        clocks = ClockSampler(clock_index)
+        clocks.start()
+        barrier(world)
+        torch.cuda.synchronize(self.dev)
+        ms = time_calls(self.step, steps, self.stream, self.dev, flush)
+        barrier(world)
+        clk = clocks.stop()
+        self.g.check_device_status(self.stream)
+        warm_ms = None
+        if flush is not None:  # the same calls back to back, inputs warm in L2
+            warm_ms = max_over_ranks(time_calls(self.step, steps, self.stream, self.dev), world)
+            self.g.check_device_status(self.stream)
+        return {"ms": ms, "ms_max": max_over_ranks(ms, world), "warm_ms": warm_ms,
+                "flushed": flush is not None, "clocks": clk}
+
+
+def attention_record(run, t, ex2, world, steps):
+    """The kernel-only part of a JSON line for an attention workload."""
+    w = run.w
+    flops, _, _ = algorithmic_counts(w, run.kv_lens)
+    rec = {"value": world * flops / (t["ms_max"] * 1e-3) / 1e12, "unit": UNIT,
+           "ms_per_step": t["ms_max"], "steps": steps,
+           "config": workload_config(w, world, flushed=t["flushed"]),
+           "gpu_launches": run.launches_per_step() * steps,
+           "roofline": attention_roofline(w, run.kv_lens, t["ms"], ex2,
+                                          attention_kernel_name_for(w)),
+           "clocks": t["clocks"]}
+    if t["warm_ms"] is not None:
+        rec["config"]["warm_l2"] = {"value": world * flops / (t["warm_ms"] * 1e-3) / 1e12,
+                                    "unit": UNIT, "ms_per_step": t["warm_ms"]}
+    return rec
+
+
+def layer_flops(w):
+    """8 N d^2 (QKV and W_O projections) + 4 N^2 d attention, causal-halved per
+    head ("Self-Attention 机制", section 瓶颈: the six matrix products)."""
+    N, dm = w.B * w.L, w.d_model
+    proj = 2.0 * N * dm * 3 * dm + 2.0 * N * dm * dm
+    attn = attn_flops(w.B, w.H, w.L, w.L, w.d_k, w.mask_kind)
+    return proj, attn
+
+
+class LayerRun:
+    """The five-step layer's inputs and weights on the device, the timed
+    layer calls, and each stage's kernel timed alone on the same shapes."""
+
+    def __init__(self, g, w, dev, stream, rank=0):
+        import torch
+        self.g, self.w, self.dev, self.stream = g, w, dev, stream
+        self.inp = make_workload_inputs(replica_workload(w, rank))
+
+        def dev_bf16(bits, pin=False):
+            t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+            return t.pin_memory() if pin else t.to(dev)
+        self.hx = dev_bf16(self.inp["x"], pin=True)
+        self.x = self.hx.to(dev)
+        self.wqkv, self.wo = dev_bf16(self.inp["w_qkv"]), dev_bf16(self.inp["w_o"])
+        self.y = torch.empty_like(self.x)
+        self.ws = torch.empty(g.mha_layer_workspace_bytes(w.B, w.L, w.d_model, w.H),
+                              dtype=torch.uint8, device=dev)
+
+    def step(self):
+        w = self.w
+        self.g.mha_layer_fwd(self.x, self.wqkv, self.wo, w.H, mask_kind=w.mask_kind,
+                             scale=w.scale, out=self.y, workspace=self.ws, stream=self.stream)
+
+    def input_bytes(self):
+        return 2 * (self.x.numel() + self.wqkv.numel() + self.wo.numel())
+
+    def time(self, steps, warmup, world=1, clock_index=0):
+        import torch
+        g, w, dev, stream = self.g, self.w, self.dev, self.stream
+        for _ in range(warmup):
+            self.step()
+        g.check_device_status(stream)
+        # X and the weights (the step's inputs) fit in L2: flush it before
+        # every timed call
+        flush = l2_flush_buffer(self.input_bytes(), dev)
+        clocks = ClockSampler(clock_index)
+        clocks.start()
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        ms = time_calls(self.step, steps, stream, dev, flush)
+        barrier(world)
+        clk = clocks.stop()
+        g.check_device_status(stream)
+        # each stage's kernel timed alone on the same shapes (for the roofline)
+        N, dm, dk = w.B * w.L, w.d_model, w.d_k
+        qkv = torch.empty((N, 3 * dm), dtype=torch.bfloat16, device=dev)
+        cat = torch.empty((N, dm), dtype=torch.bfloat16, device=dev)
+        x2 = self.x.view(N, dm)
+        ms_qkv = time_calls(lambda: g.gemm_bf16(x2, self.wqkv, out=qkv, stream=stream), steps,
+                            stream, dev, flush)
+        ms_wo = time_calls(lambda: g.gemm_bf16(cat, self.wo, out=self.y.view(N, dm),
+                                               stream=stream), steps, stream, dev, flush)
+        qh = torch.empty((w.B, w.H, w.L, dk), dtype=torch.bfloat16, device=dev).normal_()
+        kh, vh = torch.empty_like(qh).normal_(), torch.empty_like(qh).normal_()
+        oh = torch.empty_like(qh)
+        ms_att = time_calls(lambda: g.attn_fwd(qh, kh, vh, mask_kind=w.mask_kind, scale=w.scale,
+                                               out=oh, return_lse=False, stream=stream),
+                            steps, stream, dev, flush)
+        g.check_device_status(stream)
+        return {"ms": ms, "ms_max": max_over_ranks(ms, world), "flushed": flush is not None,
+                "clocks": clk, "stage_ms": {"qkv_gemm": ms_qkv, "attention": ms_att,
+                                            "wo_gemm": ms_wo}}
+
+
+def layer_record(run, t, world, steps):
+    """The kernel-only part of a JSON line for the layer workload."""
+    w = run.w
+    N, dm, dk = w.B * w.L, w.d_model, w.d_k
+    proj, attn = layer_flops(w)
+    flops = proj + attn
+    peaks, peak_src = load_peaks()
+    sm = t["stage_ms"]
+    stages = {"qkv_gemm": (2.0 * N * dm * 3 * dm, sm["qkv_gemm"]),
+              "attention": (attn, sm["attention"]), "wo_gemm": (2.0 * N * dm * dm, sm["wo_gemm"])}
+    dom = max(stages, key=lambda k: stages[k][1])
+    achieved = stages[dom][0] / (stages[dom][1] * 1e-3) / 1e12
+    kernel = {"qkv_gemm": "gemm_bf16_kernel", "wo_gemm": "gemm_bf16_kernel",
+              "attention": attention_kernel_name(w.B, w.H, w.L, dk)}[dom]
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": profiled_traffic(w.name, kernel) if dom == "attention" else None,
+                "peak_source": "%s (bf16 dense burst)" % peak_src,
+                "kernel": kernel,
+                "layer_frac": flops / (t["ms"] * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                "stages_ms": {k: v[1] for k, v in stages.items()},
+                "stages_tflops": {k: v[0] / (v[1] * 1e-3) / 1e12 for k, v in stages.items()},
+                "stages_frac": {k: v[0] / (v[1] * 1e-3) / 1e12 / peaks["bf16_tflops"]
+                                for k, v in stages.items()}}
+    cfg = {"workload": w.name, "B": w.B, "L": w.L, "d_model": dm, "H": w.H,
+           "mask": "causal" if w.mask_kind & MASK_CAUSAL else "none",
+           "parallelism": "replicas x%d" % world,
+           "l2": ("X and weights %.0f MB fit in L2: L2 flushed (a 2x L2 buffer rewritten) "
+                  "before every timed call, outside its events" % (1e-6 * run.input_bytes())
+                  if t["flushed"] else "inputs larger than L2, no flush")}
+    return {"value": world * flops / (t["ms_max"] * 1e-3) / 1e12, "unit": UNIT,
+            "ms_per_step": t["ms_max"], "steps": steps, "config": cfg,
+            "gpu_launches": 3 * steps, "roofline": roofline, "clocks": t["clocks"]}
+
+
+# The metric's other workloads, timed in the default run after the main one
+# and reported beside it: kernel-only, inputs resident, no host copies.
+EXTRA_WORKLOADS = ["mha_nomask_b1_h8_l128_d64", "mha_padding_b4_h8_l512_d64",
+                   "mha_causal_b4_h16_l4096_d128", "mha_layer_causal_b8_l2048_dm1024_h16"]
+
+
+def extra_records(g, main_name, dev, stream, args, ex2, world, clock_index):
+    out = {}
+    for name in EXTRA_WORKLOADS:
+        if name == main_name:
+            continue
+        w = WORKLOADS[name]
+        if w.kind == "layer":
+            run = LayerRun(g, w, dev, stream)
+            out[name] = layer_record(run, run.time(args.steps, args.warmup, world, clock_index),
+                                     world, args.steps)
+        else:
+            run = AttentionRun(g, w, dev, stream)
+            out[name] = attention_record(run, run.time(args.steps, args.warmup, world,
+                                                       clock_index), ex2, world, args.steps)
+        del run
+    return out
+
+
+# ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def ours_arm(args, w):
+def init_dist():
     import torch
     world, rank, local = dist_env()
     if world > 1:
@@ -372,60 +631,28 @@ def ours_arm(args, w):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
+    return world, rank, local, dev
+
+
+def ours_arm(args, w):
+    import torch
+    world, rank, local, dev = init_dist()
     import transformer_scaled_dot_sdpa_gb300 as g
-
-    inp = make_workload_inputs(replica_workload(w, rank))
-    kv_lens = inp["kv_lens"]
-
-    def pinned(bits):
-        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
-        return t.pin_memory()
-
-    hq, hk, hv = pinned(inp["q"]), pinned(inp["k"]), pinned(inp["v"])
-    q = hq.to(dev)
-    k = hk.to(dev)
-    v = hv.to(dev)
-    kvt = torch.from_numpy(kv_lens).to(dev) if kv_lens is not None else None
-    O = torch.empty((w.B, w.H, w.Lq, w.d_v), dtype=torch.bfloat16, device=dev)
-    LSE = torch.empty((w.B, w.H, w.Lq), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    decode = w.kind == "decode"
-    if decode:
-        ws = torch.empty(g.attn_decode_workspace_bytes(w.B, w.H, w.H_kv, w.Lq, w.Lk, w.d_k),
-                         dtype=torch.uint8, device=dev)
-
-    def step():
-        if decode:
-            g.attn_decode(q, k, v, mask_kind=w.mask_kind, kv_lens=kvt, scale=w.scale, out=O,
-                          lse=LSE, workspace=ws, stream=stream)
-        else:
-            g.attn_fwd(q, k, v, mask_kind=w.mask_kind, kv_lens=kvt, scale=w.scale, out=O,
-                       lse=LSE, stream=stream)
+    clock_index = dev.index if world == 1 else local
 
     ex2 = measure_ex2_rate(g, dev, stream)  # denominator of the roofline's exp term
-    for _ in range(args.warmup):
-        step()
-    g.check_device_status(stream)
-
-    flush = l2_flush_buffer(attn_input_bytes(w), dev)
-    clocks = ClockSampler(dev.index if world == 1 else local)
-    clocks.start()
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    ms = time_calls(step, args.steps, stream, dev, flush)
-    barrier(world)
-    clk = clocks.stop()
-    g.check_device_status(stream)
-    ms_max = max_over_ranks(ms, world)
-    warm_ms = None
-    if flush is not None:  # the same calls back to back, inputs warm in L2
-        warm_ms = max_over_ranks(time_calls(step, args.steps, stream, dev), world)
-        g.check_device_status(stream)
+    run = AttentionRun(g, w, dev, stream, rank)
+    t = run.time(args.steps, args.warmup, world, clock_index)
+    rec = attention_record(run, t, ex2, world, args.steps)
+    decode = run.decode
+    kv_lens = run.kv_lens
+    hq, hk, hv, k, v = run.hq, run.hk, run.hv, run.k, run.v
 
     # end to end through the public API with host buffers: pinned H2D of the
     # inputs, the attention call, D2H of O and LSE, every step
-    hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
-    hL = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
+    hO = torch.empty(run.O.shape, dtype=run.O.dtype).pin_memory()
+    hL = torch.empty(run.LSE.shape, dtype=run.LSE.dtype).pin_memory()
     e2e_steps = max(1, min(args.steps, 10))
 
     if decode:
@@ -445,6 +672,8 @@ def ours_arm(args, w):
         dws = torch.empty(max(256, g.attn_decode_host_workspace_bytes(w.B, w.H, w.H_kv, w.Lq,
                                                                       w.Lk, w.d_k)),
                           dtype=torch.uint8, device=dev)
+        h2d = hq.numel() * 2 + hk_new.numel() * 2 + hv_new.numel() * 2 + (
+            4 * w.B if w.mask_kind & MASK_PADDING else 0)
 
         def e2e_step():
             g.attn_decode_host(hq, hk_new, hv_new, k, v, mask_kind=w.mask_kind,
@@ -458,6 +687,7 @@ def ours_arm(args, w):
         hws = torch.empty(max(256, g.attn_fwd_host_workspace_bytes(w.B, w.H, w.H, w.Lq, w.Lk,
                                                                    w.d_k, w.d_v)),
                           dtype=torch.uint8, device=dev)
+        h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
 
         def e2e_step():
             g.attn_fwd_host(hq, hk, hv, mask_kind=w.mask_kind, kv_lens=hkv, scale=w.scale, out=hO,
@@ -482,35 +712,13 @@ def ours_arm(args, w):
         e2e_windows.append(max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world))
     e2e_ms = statistics.median(e2e_windows)
     g.check_device_status(stream)
+    flops, _, _ = algorithmic_counts(w, kv_lens)
+    inp = run.inp
+    del run, k, v
 
-    flops, exps, hbm_bytes = algorithmic_counts(w, kv_lens)
-    value = world * flops / (ms_max * 1e-3) / 1e12
-    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
-    peaks, peak_src = load_peaks()
-    tensor_peak = peaks["bf16_tflops"] * 1e12
-    hbm_peak = peaks["hbm_gbs"] * 1e9
-    t_tensor = flops / tensor_peak
-    t_exp = exps / ex2["exp_per_s"]
-    t_hbm = hbm_bytes / hbm_peak
-    bound = max((t_tensor, "tensor"), (t_hbm, "hbm"), (t_exp, "exp"))[1]
-    achieved_tflops = flops / (ms * 1e-3) / 1e12   # this rank's kernel
-    kernel = ("attn_fwd_split_kernel<%d> (decode mode)" % w.d_k if w.kind == "decode"
-              else attention_kernel_name(w.B, w.H, w.Lq, w.d_k))
-    roofline = {
-        "bound": "tensor" if bound in ("tensor", "exp") else "hbm",
-        "achieved": achieved_tflops if bound != "hbm" else hbm_bytes / (ms * 1e-3) / 1e9,
-        "peak": peaks["bf16_tflops"] if bound != "hbm" else peaks["hbm_gbs"],
-        "unit": "TFLOP/s" if bound != "hbm" else "GB/s",
-        "peak_source": "%s (bf16 dense burst)" % peak_src if bound != "hbm" else peak_src,
-        "kernel": kernel,
-        "traffic": profiled_traffic(w.name, kernel),
-        "roofline_time_ms": 1e3 * max(t_tensor, t_exp, t_hbm),
-        "frac_of_roofline_time": 1e3 * max(t_tensor, t_exp, t_hbm) / ms,
-        "exp_bound_fraction": t_exp / max(t_tensor, t_hbm),
-        "exp_rate": {"exp_per_s": ex2["exp_per_s"], "exp_per_clk_per_sm": ex2["exp_per_clk_per_sm"],
-                     "sm_mhz": ex2["sm_mhz"], "source": "measured (attn_probe_ex2)"},
-    }
-    roofline["frac"] = roofline["achieved"] / roofline["peak"]
+    extra = None
+    if not args.no_extra:
+        extra = extra_records(g, w.name, dev, stream, args, ex2, world, clock_index)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -520,27 +728,22 @@ def ours_arm(args, w):
                          % (n, w.B * w.H, fl, dt)}
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(w, world, flushed=flush is not None),
-        "e2e": {"value": e2e_value, "unit": UNIT,
-                "h2d_bytes_per_step": int(hq.numel() * 2 + (hk_new.numel() * 2 + hv_new.numel() * 2
-                                                             + (4 * w.B if w.mask_kind & MASK_PADDING
-                                                                else 0)
-                                                             if decode else
-                                                             hk.numel() * 2 + hv.numel() * 2)),
+        "metric": METRIC, "value": rec["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": rec["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": rec["config"],
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(hO.numel() * 2 + hL.numel() * 4),
                 "steps": e2e_steps, "ms_per_step": e2e_ms, "windows_ms_per_step": e2e_windows,
                 "api": e2e_api},
-        "gpu_launches": (2 if w.kind == "decode" else 1) * args.steps,
-        "roofline": roofline,
+        "gpu_launches": rec["gpu_launches"],
+        "roofline": rec["roofline"],
         "cpu_baseline": cpu,
-        "clocks": clk,
+        "clocks": rec["clocks"],
     }
-    if warm_ms is not None:
-        line["config"]["warm_l2"] = {"value": world * flops / (warm_ms * 1e-3) / 1e12,
-                                     "unit": UNIT, "ms_per_step": warm_ms}
+    if extra is not None:
+        line["workloads"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -552,42 +755,14 @@ def ours_arm(args, w):
 # ---------------------------------------------------------------------------
 # the five-step layer workload
 # ---------------------------------------------------------------------------
-def layer_flops(w):
-    """8 N d^2 (QKV and W_O projections) + 4 N^2 d attention, causal-halved per
-    head ("Self-Attention 机制", section 瓶颈: the six matrix products)."""
-    N, dm = w.B * w.L, w.d_model
-    proj = 2.0 * N * dm * 3 * dm + 2.0 * N * dm * dm
-    attn = attn_flops(w.B, w.H, w.L, w.L, w.d_k, w.mask_kind)
-    return proj, attn
-
-
 def layer_arm(args, w):
     import torch
-    world, rank, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
+    world, rank, local, dev = init_dist()
     import transformer_scaled_dot_sdpa_gb300 as g
-    inp = make_workload_inputs(replica_workload(w, rank))
-
-    def dev_bf16(bits, pin=False):
-        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
-        return t.pin_memory() if pin else t.to(dev)
-
-    hx = dev_bf16(inp["x"], pin=True)
-    x = hx.to(dev)
-    wqkv, wo = dev_bf16(inp["w_qkv"]), dev_bf16(inp["w_o"])
-    y = torch.empty_like(x)
-    ws = torch.empty(g.mha_layer_workspace_bytes(w.B, w.L, w.d_model, w.H), dtype=torch.uint8,
-                     device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    def step():
-        g.mha_layer_fwd(x, wqkv, wo, w.H, mask_kind=w.mask_kind, scale=w.scale, out=y,
-                        workspace=ws, stream=stream)
+    run = LayerRun(g, w, dev, stream, rank)
+    t = run.time(args.steps, args.warmup, world, dev.index if world == 1 else local)
+    rec = layer_record(run, t, world, args.steps)
 
     def timed(fn, n):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -599,71 +774,28 @@ def layer_arm(args, w):
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) / n
 
-    for _ in range(args.warmup):
-        step()
-    g.check_device_status(stream)
-    # X and the weights (the step's inputs) fit in L2: flush it before every
-    # timed call
-    flush = l2_flush_buffer(2 * (x.numel() + wqkv.numel() + wo.numel()), dev)
-    clocks = ClockSampler(dev.index if world == 1 else local)
-    clocks.start()
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    ms = time_calls(step, args.steps, stream, dev, flush)
-    barrier(world)
-    clk = clocks.stop()
-    g.check_device_status(stream)
-    ms_max = max_over_ranks(ms, world)
-
-    # each stage's kernel timed alone on the same shapes (for the roofline)
-    N, dm, dk = w.B * w.L, w.d_model, w.d_k
-    qkv = torch.empty((N, 3 * dm), dtype=torch.bfloat16, device=dev)
-    cat = torch.empty((N, dm), dtype=torch.bfloat16, device=dev)
-    x2 = x.view(N, dm)
-    ms_qkv = time_calls(lambda: g.gemm_bf16(x2, wqkv, out=qkv, stream=stream), args.steps, stream,
-                        dev, flush)
-    ms_wo = time_calls(lambda: g.gemm_bf16(cat, wo, out=y.view(N, dm), stream=stream), args.steps,
-                       stream, dev, flush)
-    qh = torch.empty((w.B, w.H, w.L, dk), dtype=torch.bfloat16, device=dev).normal_()
-    kh, vh = torch.empty_like(qh).normal_(), torch.empty_like(qh).normal_()
-    oh = torch.empty_like(qh)
-    ms_att = time_calls(lambda: g.attn_fwd(qh, kh, vh, mask_kind=w.mask_kind, scale=w.scale,
-                                           out=oh, return_lse=False, stream=stream),
-                        args.steps, stream, dev, flush)
-    g.check_device_status(stream)
-
     # end to end: X in from pinned host memory, Y back, every step, through
     # the library's host-buffer layer call (copies overlapped with the
     # kernels over chunks of batch elements); the weights stay on the device
-    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    hx = run.hx
+    hy = torch.empty(run.y.shape, dtype=run.y.dtype).pin_memory()
     hws = torch.empty(max(256, g.mha_layer_host_workspace_bytes(w.B, w.L, w.d_model, w.H)),
                       dtype=torch.uint8, device=dev)
     e2e_steps = max(1, min(args.steps, 10))
 
     def e2e_step():
-        g.mha_layer_fwd_host(hx, wqkv, wo, w.H, mask_kind=w.mask_kind, scale=w.scale, out=hy,
-                             workspace=hws, stream=stream)
+        g.mha_layer_fwd_host(hx, run.wqkv, run.wo, w.H, mask_kind=w.mask_kind, scale=w.scale,
+                             out=hy, workspace=hws, stream=stream)
 
     e2e_step()
     e2e_windows = [max_over_ranks(timed(e2e_step, e2e_steps), world) for _ in range(E2E_WINDOWS)]
     e2e_ms = statistics.median(e2e_windows)
+    g.check_device_status(stream)
 
     proj, attn = layer_flops(w)
     flops = proj + attn
-    peaks, peak_src = load_peaks()
-    stages = {"qkv_gemm": (2.0 * N * dm * 3 * dm, ms_qkv), "attention": (attn, ms_att),
-              "wo_gemm": (2.0 * N * dm * dm, ms_wo)}
-    dom = max(stages, key=lambda k: stages[k][1])
-    achieved = stages[dom][0] / (stages[dom][1] * 1e-3) / 1e12
-    kernel = {"qkv_gemm": "gemm_bf16_kernel", "wo_gemm": "gemm_bf16_kernel",
-              "attention": attention_kernel_name(w.B, w.H, w.L, dk)}[dom]
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                "traffic": profiled_traffic(w.name, kernel) if dom == "attention" else None,
-                "peak_source": "%s (bf16 dense burst)" % peak_src,
-                "kernel": kernel,
-                "stages_ms": {k: v[1] for k, v in stages.items()},
-                "stages_tflops": {k: v[0] / (v[1] * 1e-3) / 1e12 for k, v in stages.items()}}
+    dm, dk = w.d_model, w.d_k
+    inp = run.inp
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -680,25 +812,18 @@ def layer_arm(args, w):
                "kind": "oracle", "sample": "%d output rows of one sequence (K/V projections of "
                "the whole sequence), %.3g FLOP in %.1f s" % (len(rows), fl, dt)}
     line = {
-        "metric": METRIC, "value": world * flops / (ms_max * 1e-3) / 1e12, "unit": UNIT,
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "L": w.L, "d_model": dm, "H": w.H,
-                   "mask": "causal" if w.mask_kind & MASK_CAUSAL else "none",
-                   "parallelism": "replicas x%d" % world,
-                   "l2": ("X and weights %.0f MB fit in L2: L2 flushed (a 2x L2 buffer "
-                          "rewritten) before every timed call, outside its events"
-                          % (2e-6 * (x.numel() + wqkv.numel() + wo.numel()))
-                          if flush is not None else "inputs larger than L2, no flush")},
+        "metric": METRIC, "value": rec["value"], "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": rec["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": rec["config"],
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(hx.numel() * 2), "d2h_bytes_per_step": int(hy.numel() * 2),
                 "steps": e2e_steps, "ms_per_step": e2e_ms, "windows_ms_per_step": e2e_windows,
                 "api": "mha_layer_fwd_host (copies overlapped with the kernels)"},
-        "gpu_launches": 3 * args.steps,
-        "roofline": roofline,
+        "gpu_launches": rec["gpu_launches"],
+        "roofline": rec["roofline"],
         "cpu_baseline": cpu,
-        "clocks": clk,
+        "clocks": rec["clocks"],
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -720,6 +845,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=512,
                     help="query rows per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time the named workload only, without the other workloads' records")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
