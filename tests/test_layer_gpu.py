@@ -72,13 +72,12 @@ def test_layer_small(cuda_lib, schedule, B, L, dm, H, mask):
 def test_layer_workload_sampled(cuda_lib, schedule):
     """The full layer workload (B=8, L=2048, d_model=1024, 16 heads, causal)
     in the benchmark's launch configuration; the oracle computes sampled rows
-    of two sequences."""
+    of every one of the 8 sequences (a different sample in each)."""
     w = WORKLOADS["mha_layer_causal_b8_l2048_dm1024_h16"]
     inp = make_workload_inputs(w)
     Y = _layer_run(cuda_lib, inp, w.H, w.mask_kind)
     assert np.all(np.isfinite(Y))
-    rows = sample_rows(w.L, 40, seed=w.seed)
-    flat = np.concatenate([0 * w.L + rows, 5 * w.L + rows])
+    flat = np.concatenate([b * w.L + sample_rows(w.L, 24, seed=w.seed + b) for b in range(w.B)])
     Yr = oracle.mha_layer(inp["x"], inp["w_qkv"], inp["w_o"], w.H, mask_kind=w.mask_kind,
                           rows=flat)
     _compare(Y.reshape(-1, w.d_model)[flat], Yr, w.name)
