@@ -62,6 +62,9 @@ constexpr int ATTN_QTILES = 2;     // Q tiles per work item
 constexpr int ATTN_ROWS_PER_ITEM = ATTN_BLOCK_M * ATTN_QTILES;
 constexpr uint32_t ATTN_TMEM_COLS = 512;
 constexpr float ATTN_RESCALE_THRESHOLD = 8.0f;  // log2 units
+// Q tile 0 takes the lower 128 rows of even items and the upper 128 of odd
+// ones (see attn_get_item)
+constexpr bool ATTN_ALTERNATE_TILES = true;
 
 enum : unsigned int { ATTN_STATUS_TIMEOUT = 1u, ATTN_STATUS_BAD_KVLEN = 2u };
 enum : int { ATTN_MASK_CAUSAL_BIT = 1, ATTN_MASK_PADDING_BIT = 2 };
@@ -219,6 +222,15 @@ __device__ __forceinline__ bool attn_get_item(const AttnParams& p, int k, AttnIt
     }
     it.nkv[t] = n;
     it.nkv_max = max(it.nkv_max, n);
+  }
+  if (ATTN_ALTERNATE_TILES && (k & 1)) {
+    // the upper 128 rows of a causal block need one key tile more than the
+    // lower ones: the two Q tiles take them in turn, item by item
+    const int r = it.row0[0], n = it.nkv[0];
+    it.row0[0] = it.row0[1];
+    it.nkv[0] = it.nkv[1];
+    it.row0[1] = r;
+    it.nkv[1] = n;
   }
   return true;
 }
