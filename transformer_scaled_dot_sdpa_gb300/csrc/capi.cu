@@ -320,8 +320,19 @@ attn_status_t run_gemm(DeviceState* ds, const void* A, const void* Bm, void* C, 
     std::lock_guard<std::mutex> lock(g_mutex);
     p.wait_limit_ns = g_wait_limit_ns;
   }
+  // A last wave that would leave pairs idle is run as half-width tiles when
+  // those still fit in one wave: it then takes half as long.  Measured with
+  // L2 flushed: 16384 x 1024 x 1024 (256 tiles on 76 pairs, 28 in the last
+  // wave) and 16384 x 3072 x 1024 (768 tiles, 8 in the last wave).
   const int tiles = p.m_tiles * p.n_tiles;
-  const int pairs = tiles < ds->gemm_pairs ? tiles : ds->gemm_pairs;
+  const int rem = tiles % ds->gemm_pairs;
+  p.n_full = tiles;
+  p.n_list = tiles;
+  if (rem != 0 && 2 * rem <= ds->gemm_pairs) {
+    p.n_full = tiles - rem;
+    p.n_list = p.n_full + 2 * rem;
+  }
+  const int pairs = p.n_list < ds->gemm_pairs ? p.n_list : ds->gemm_pairs;
   gb300::gemm_bf16_kernel<<<2 * pairs, gb300::GEMM_THREADS, gb300::GemmLayout::SMEM_BYTES,
                             stream>>>(ma, mb, mc, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

@@ -49,16 +49,32 @@ struct GemmLayout {
 struct GemmParams {
   int M, N, K;
   int m_tiles, n_tiles, k_blocks;
+  // The tile list: the first n_full tiles of the M-fastest order at full
+  // width, then the rest split into two halves of GEMM_BN / 2 columns each
+  // (entries n_full + 2 i and n_full + 2 i + 1), n_list entries in all.
+  // The host splits the tiles of a last, partial wave when the halves still
+  // fit in one wave, so that wave takes half as long.
+  int n_full, n_list;
   __nv_bfloat16* C;
   unsigned int* status;
   unsigned long long wait_limit_ns;
 };
 
-__device__ __forceinline__ void gemm_tile_coords(const GemmParams& p, int tile, int& m0, int& n0) {
-  const int mt = tile % p.m_tiles;
-  const int nt = tile / p.m_tiles;
+// Output corner of list entry `tile`; returns its width in columns.
+__device__ __forceinline__ int gemm_tile_coords(const GemmParams& p, int tile, int& m0, int& n0) {
+  int t = tile, half = -1;
+  if (tile >= p.n_full) {
+    const int h = tile - p.n_full;
+    t = p.n_full + (h >> 1);
+    half = h & 1;
+  }
+  const int mt = t % p.m_tiles;
+  const int nt = t / p.m_tiles;
   m0 = mt * GEMM_BM;
   n0 = nt * GEMM_BN;
+  if (half < 0) return GEMM_BN;
+  n0 += half * (GEMM_BN / 2);
+  return GEMM_BN / 2;
 }
 
 // One cluster = one pair of CTAs on a TPC; the pair computes 256 x 256 output
@@ -97,7 +113,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: its peer
   const int pair = static_cast<int>(blockIdx.x >> 1);
   const int n_pairs = static_cast<int>(gridDim.x >> 1);
-  const int n_tiles_total = p.m_tiles * p.n_tiles;
+  const int n_tiles_total = p.n_list;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < GEMM_STAGES; ++s) {
@@ -134,9 +150,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       bool ok = true;
       for (int tile = pair; ok && tile < n_tiles_total; tile += n_pairs) {
         int m0, n0;
-        gemm_tile_coords(p, tile, m0, n0);
+        const int cw = gemm_tile_coords(p, tile, m0, n0) / 2;  // B columns this CTA stages
         const int row = m0 + static_cast<int>(rank) * GEMM_BM_CTA;
-        const int col = n0 + static_cast<int>(rank) * GEMM_BN_CTA;
+        const int col = n0 + static_cast<int>(rank) * cw;
         for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
           const int s = static_cast<int>(it % GEMM_STAGES);
           if (it >= static_cast<uint32_t>(GEMM_STAGES)) {
@@ -147,11 +163,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
           // odd CTA's bytes may land before this expect_tx (the count then
           // runs below zero until it does, and the phase cannot complete
           // without this arrival)
-          if (rank == 0) mbar_arrive_expect_tx(&bars[L::B_FULL + s], 2 * L::STAGE_BYTES);
+          if (rank == 0)
+            mbar_arrive_expect_tx(&bars[L::B_FULL + s], 2 * (L::A_BYTES + (cw / 64) * L::B_CHUNK));
           const uint32_t fb = full0 + static_cast<uint32_t>(s) * 8u;
           tma_load_2d_pair(smem + L::A_OFF + s * L::A_BYTES, &tmA, fb, kb * GEMM_BK, row);
-#pragma unroll
-          for (int c = 0; c < GEMM_BN_CTA / 64; ++c)
+          for (int c = 0; c < cw / 64; ++c)
             tma_load_2d_pair(smem + L::B_OFF + s * L::B_BYTES + c * L::B_CHUNK, &tmB, fb,
                              col + 64 * c, kb * GEMM_BK);
         }
@@ -172,6 +188,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       // The whole warp waits and computes operands; one elected lane issues,
       // so the operands stay warp-uniform and each MMA issues quickly.
       constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, GEMM_BN, true);
+      constexpr uint32_t IDESC_HALF = idesc_bf16_f32(GEMM_BM, GEMM_BN / 2, true);
       constexpr unsigned FULL = 0xffffffffu;
       constexpr uint16_t BOTH = 0x3;
       const uint64_t a_desc = smem_desc_sw128(smem_u32(smem + L::A_OFF), 16, 1024);
@@ -186,6 +203,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
           tc_fence_after();
         }
         const uint32_t d_tmem = tmem + acc * GEMM_BN;
+        int m0, n0;
+        const uint32_t idesc =
+            gemm_tile_coords(p, tile, m0, n0) == GEMM_BN ? IDESC : IDESC_HALF;
         for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
           const int s = static_cast<int>(it % GEMM_STAGES);
           ok = __all_sync(FULL, mbar_wait(&bars[L::B_FULL + s], (it / GEMM_STAGES) & 1u, ctl));
@@ -197,7 +217,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < GEMM_BK / 16; ++kk)
               mma_bf16_ss_pair(d_tmem, ad + static_cast<uint64_t>((kk * 32) >> 4),
-                               bd + static_cast<uint64_t>((kk * 2048) >> 4), IDESC,
+                               bd + static_cast<uint64_t>((kk * 2048) >> 4), idesc,
                                (kb > 0 || kk > 0) ? 1u : 0u);
             mma_commit_pair_multicast(&bars[L::B_EMPTY + s], BOTH);
           }
@@ -226,12 +246,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       int m0, n0;
-      gemm_tile_coords(p, tile, m0, n0);
+      const int width = gemm_tile_coords(p, tile, m0, n0);
       const int box_row = m0 + static_cast<int>(rank) * GEMM_BM_CTA + wq * 32;
       // M is a multiple of 128: a box of 32 rows lies wholly inside or past M
       const bool rows_in = box_row < p.M;
 #pragma unroll 1
-      for (int c = 0; c < GEMM_BN / 64; ++c) {
+      for (int c = 0; c < width / 64; ++c) {
         uint32_t r0[32], r1[32];
         tmem_ld_32x32b_x32(tmem + acc * GEMM_BN + lane_base + c * 64u, r0);
         tmem_ld_32x32b_x32(tmem + acc * GEMM_BN + lane_base + c * 64u + 32u, r1);
