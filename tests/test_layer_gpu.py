@@ -21,14 +21,19 @@ def _gemm_case(M, N, K, seed):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 192), (384, 768, 1024),
-                                   (640, 256, 64), (1024, 3072, 1024), (8192, 4096, 512)])
+                                   (640, 256, 64), (1024, 3072, 1024), (8192, 4096, 512),
+                                   (8192, 2560, 256), (2176, 1024, 128)])
 def test_gemm_matches_fp64_matmul(cuda_lib, M, N, K):
     """C = A B: bf16 inputs, fp32 accumulation, one bf16 rounding of the
     result.  The fp64 product of the same bf16 values (a library matmul) is
     the reference; the bound is half a bf16 ulp (2^-8 relative) plus fp32
     accumulation slack.  The shapes cover a pair whose second 128 rows lie
-    past M (M = 128, 384, 640) and, at 8192 x 4096, several 256 x 256 tiles
-    per CTA pair, so both TMEM accumulators are reused."""
+    past M (M = 128, 384, 640, 2176) and, at 8192 x 4096, several 256 x 256
+    tiles per CTA pair, so both TMEM accumulators are reused.  On a GPU with
+    76 CTA pairs, the tiles of a last, partial wave run as half-width tiles
+    when those fit in one wave: all tiles for the shapes of up to 38 tiles
+    (2176 x 1024: 36), the last 16 of 320 at 8192 x 2560; not at
+    1024 x 3072 (48 in the one wave) or 8192 x 4096 (56 in the last)."""
     a, b = _gemm_case(M, N, K, seed=M + N + K)
     C = down(cuda_lib.gemm_bf16(up(a), up(b)))
     cuda_lib.check_device_status()
