@@ -161,7 +161,9 @@ static int valid_keys(int i, int Lq, int Lk, int mask_kind, int kv_len)
         long long pos = (long long)n_seq - (long long)Lq + (long long)i;
         if (pos < 0)
             return 0; /* the query precedes the sequence: no keys, output 0 */
-        return (int)(pos + 1); /* keys 0..p_i; p_i < n_seq because i < Lq */
+        /* keys 0..p_i; p_i < n_seq because i < Lq (the bound only guards the
+           buffers against a wrong offset) */
+        return (pos + 1 < n) ? (int)(pos + 1) : n;
     }
     if (padding && i >= kv_len)
         return 0; /* padded query row: output 0 */
@@ -502,6 +504,8 @@ done:
  * oracle_mha_layer: see the file header for the definition.
  *   X [B,L,dm], Wqkv [dm, 3*dm], Wo [dm, dm]: bf16 bit patterns, contiguous.
  *   H heads, d_k = dm / H (dm must be divisible by H).
+ *   mask_kind: CAUSAL, CAUSAL_BR (exclusive with CAUSAL), PADDING, as for the
+ *         attention (Lq = Lk = L).
  *   rows: flat ids b*L + l of the output rows wanted (any order), or NULL
  *         for all B*L rows.  Y [nrows, dm] fp64.
  */
@@ -514,7 +518,9 @@ int oracle_mha_layer(const uint16_t *X, const uint16_t *Wqkv, const uint16_t *Wo
     int64_t r;
     if (!X || !Wqkv || !Wo || !Y || B < 0 || L < 0 || dm < 1 || H < 1 || dm % H != 0)
         return OR_ERR_ARG;
-    if ((mask_kind & ~(OR_MASK_CAUSAL | OR_MASK_PADDING)) != 0)
+    if ((mask_kind & ~(OR_MASK_CAUSAL | OR_MASK_PADDING | OR_MASK_CAUSAL_BR)) != 0)
+        return OR_ERR_ARG;
+    if ((mask_kind & OR_MASK_CAUSAL) && (mask_kind & OR_MASK_CAUSAL_BR))
         return OR_ERR_ARG;
     if (mask_kind & OR_MASK_PADDING) {
         if (!kv_lens)

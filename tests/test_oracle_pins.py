@@ -563,6 +563,36 @@ def layer_matches_torch_multi_head_attention(orc):
 
 
 @pin
+def layer_bottom_right_causal_with_padding_matches_torch(orc):
+    """The layer under the bottom-right causal mask: without padding it is the
+    ordinary causal layer (Lq = Lk), bit for bit; with per-sequence lengths,
+    row i of sequence b attends to the keys j <= kv_len_b - L + i, checked
+    against PyTorch's multi_head_attention_forward in float64 with that mask
+    written out for each sequence (rows with no key give Y = 0)."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    BR = 4
+    x, wqkv, wo = _layer_case(151)
+    B, L, dm, H = 2, 19, 24, 3
+    a = orc.mha_layer(x, wqkv, wo, H, mask_kind=BR)
+    c = orc.mha_layer(x, wqkv, wo, H, mask_kind=MASK_CAUSAL)
+    assert np.array_equal(a, c)
+    kv = np.array([19, 7], dtype=np.int32)
+    Y = orc.mha_layer(x, wqkv, wo, H, mask_kind=BR | MASK_PADDING, kv_lens=kv)
+    for b in range(B):
+        keep = np.arange(L)[None, :] <= (kv[b] - L + np.arange(L))[:, None]
+        live = keep.any(axis=1)
+        xt = torch.from_numpy(_widen(x[b:b + 1])).transpose(0, 1)
+        ty, _ = F.multi_head_attention_forward(
+            xt, xt, xt, dm, H, torch.from_numpy(_widen(wqkv)).T.contiguous(), None, None, None,
+            False, 0.0, torch.from_numpy(_widen(wo)).T.contiguous(), None, training=False,
+            need_weights=False, attn_mask=torch.from_numpy(~keep))
+        ty = ty.transpose(0, 1).numpy()[0]
+        np.testing.assert_allclose(Y[b][live], ty[live], atol=1e-12)
+        assert np.all(Y[b][~live] == 0.0)
+
+
+@pin
 def layer_with_identity_weights_is_attention(orc):
     """One head, W_QKV = [I | I | I], W_O = I: the layer is plain attention of
     X with itself -- the worked example of P-a 六 / P-d again."""
@@ -672,12 +702,10 @@ MUTANTS = [
     ("causal_br_offset_from_cache_size",
      "long long pos = (long long)n_seq - (long long)Lq + (long long)i;\n"
      "        if (pos < 0)\n"
-     "            return 0; /* the query precedes the sequence: no keys, output 0 */\n"
-     "        return (int)(pos + 1);",
+     "            return 0; /* the query precedes the sequence: no keys, output 0 */",
      "long long pos = (long long)Lk - (long long)Lq + (long long)i;\n"
      "        if (pos < 0 || (padding && i >= kv_len))\n"
-     "            return 0;\n"
-     "        return (pos + 1 < n) ? (int)(pos + 1) : n;"),
+     "            return 0;"),
     ("layer_wo_transposed", "J.Wo_d[(size_t)c * dm + n] = widen_bf16(Wo[(size_t)c * dm + n]);",
      "J.Wo_d[(size_t)n * dm + c] = widen_bf16(Wo[(size_t)c * dm + n]);"),
 ]
