@@ -74,6 +74,21 @@ def test_layer_small(cuda_lib, schedule, B, L, dm, H, mask):
             assert np.all(Y[b, kv[b]:] == 0.0)
 
 
+def test_layer_bottom_right_causal_with_padding(cuda_lib, schedule):
+    """The layer under the bottom-right causal mask with per-sequence lengths:
+    sequence b's rows end at its own length, so rows before L - kv_len_b see
+    no key and give Y = 0, and row i sees the keys up to kv_len_b - L + i."""
+    B, L, dm, H = 3, 384, 512, 8  # B * L a multiple of 128
+    mask = 4 | MASK_PADDING
+    inp = make_layer_inputs(B, L, dm, seed=733, w_std=1.0 / np.sqrt(dm))
+    kv = np.array([L, 200, 1], dtype=np.int32)
+    Y = _layer_run(cuda_lib, inp, H, mask, kv)
+    Yr = oracle.mha_layer(inp["x"], inp["w_qkv"], inp["w_o"], H, mask_kind=mask, kv_lens=kv)
+    _compare(Y, Yr, "layer bottom-right causal + padding")
+    for b in range(B):
+        assert np.all(Y[b, :L - kv[b]] == 0.0) and np.any(Y[b, L - kv[b]:] != 0.0)
+
+
 def test_layer_workload_sampled(cuda_lib, schedule):
     """The full layer workload (B=8, L=2048, d_model=1024, 16 heads, causal)
     in the benchmark's launch configuration; the oracle computes sampled rows

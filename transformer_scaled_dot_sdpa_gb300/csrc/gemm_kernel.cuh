@@ -49,7 +49,7 @@ struct GemmLayout {
 struct GemmParams {
   int M, N, K;
   int m_tiles, n_tiles, k_blocks;
-  // The tile list: the first n_full tiles of the M-fastest order at full
+  // The tile list: the first n_full tiles of the N-fastest order at full
   // width, then the rest split into two halves of GEMM_BN / 2 columns each
   // (entries n_full + 2 i and n_full + 2 i + 1), n_list entries in all.
   // The host splits the tiles of a last, partial wave when the halves still
@@ -68,8 +68,10 @@ __device__ __forceinline__ int gemm_tile_coords(const GemmParams& p, int tile, i
     t = p.n_full + (h >> 1);
     half = h & 1;
   }
-  const int mt = t % p.m_tiles;
-  const int nt = t / p.m_tiles;
+  // N-fastest: the pairs of a wave share few rows of A, so the first wave
+  // does not read all of A from DRAM at once
+  const int mt = t / p.n_tiles;
+  const int nt = t % p.n_tiles;
   m0 = mt * GEMM_BM;
   n0 = nt * GEMM_BN;
   if (half < 0) return GEMM_BN;
