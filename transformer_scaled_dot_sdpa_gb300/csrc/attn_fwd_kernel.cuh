@@ -725,6 +725,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns, ATTN_STATUS_TIMEOUT};
+  // Set-up done (on-chip only).  Behind a dependent launch this overlapped
+  // the previous kernel's tail; nothing in global memory is touched before
+  // that kernel has completed.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   // Register split: the two softmax warpgroups take 216 registers per
   // thread, the control warpgroup (MMA, TMA and two idle warps) 72; together

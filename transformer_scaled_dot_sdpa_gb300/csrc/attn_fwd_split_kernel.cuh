@@ -723,6 +723,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns, ATTN_STATUS_TIMEOUT};
+  // Set-up done (on-chip only).  Behind a dependent launch this overlapped
+  // the previous kernel's tail; nothing in global memory is touched before
+  // that kernel has completed.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   // Register split as in attn_fwd_kernel: softmax warpgroups 216, control 72;
   // together exactly the 384 x 168 registers of the launch.
@@ -770,6 +775,8 @@ __global__ void __launch_bounds__(128)
                                __nv_bfloat16* __restrict__ O, float* __restrict__ LSE) {
   constexpr int PER = D / 32;
   constexpr unsigned FULL = 0xffffffffu;
+  grid_dependency_wait();  // the partial results of the kernel ahead of it
+  grid_launch_dependents();
   const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31u);
   if (row >= rows) return;  // uniform over the warp

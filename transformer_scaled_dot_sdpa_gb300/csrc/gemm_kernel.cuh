@@ -141,6 +141,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns, GEMM_STATUS_TIMEOUT};
+  // Set-up done (on-chip only).  Behind a dependent launch this overlapped
+  // the previous kernel's tail; nothing in global memory is touched before
+  // that kernel has completed.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {

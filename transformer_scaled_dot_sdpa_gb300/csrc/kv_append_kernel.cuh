@@ -8,6 +8,8 @@
 
 #include <cstdint>
 
+#include "ptx.cuh"
+
 namespace gb300 {
 
 // knew, vnew: [B, h_kv, Lq, d] staged new rows; K, V: [B, h_kv, Lk, d] caches;
@@ -19,6 +21,8 @@ __global__ void __launch_bounds__(256)
                      uint4* __restrict__ K, uint4* __restrict__ V,
                      const int32_t* __restrict__ kv_lens, int B, int h_kv, int Lq, int Lk,
                      int pieces_per_row) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const long long n = static_cast<long long>(B) * h_kv * Lq * pieces_per_row;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {

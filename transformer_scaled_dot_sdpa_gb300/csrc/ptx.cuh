@@ -174,6 +174,18 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream serialization attribute may start before the kernel ahead of it in
+// the stream has finished; grid_dependency_wait() returns once that kernel
+// has completed and its writes are visible (at once for a plain launch).
+// grid_launch_dependents() lets the kernel behind this one launch early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // shared::cluster address of the object at shared::cta address `addr` in the
 // CTA of rank `rank` of this cluster
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
