@@ -27,8 +27,9 @@
 //            [256,384) O accumulator of tile 0, [384,512) O of tile 1
 //   D = 64:  [256,320) O of tile 0, [320,384) O of tile 1, and P has columns
 //            of its own: [384,448) P of tile 0, [448,512) P of tile 1
-// Each Q tile has its own MMA issuer; while one softmax group works on its
-// S, the tensor core runs the other tile's P.V and next S.  At D = 64 the
+// Each Q tile has its own MMA issuer, and at D = 128 the two take turns: while
+// one softmax group works on its S, the tensor core runs the other tile's P.V
+// and next S.  At D = 64 the
 // separate P columns also let S_t(j+1) start as soon as the softmax has read
 // S_t(j) ("early S"), so it overlaps that softmax's exponentials.
 //
@@ -37,7 +38,8 @@
 // fp32 probabilities (gives the LSE) and lb of the bf16-rounded
 // probabilities that the tensor core multiplies into V (normalises O, so
 // O / lb is an exactly normalised average of V rows and a one-hot row
-// reproduces its V row).  The max used
+// reproduces its V row; normalised by l instead, the peaked long-context
+// rows drift just past the 1.5e-2 bound on O).  The max used
 // for the exponentials is only moved when it grows by more than 8 (a factor
 // 256); otherwise the stale max is kept, which is exact after the final
 // division by l because O and l share it.
@@ -134,14 +136,19 @@ struct AttnLayout {
   static constexpr int B_Q_EMPTY = 2;
   static constexpr int B_K_FULL = 4;
   static constexpr int B_V_FULL = B_K_FULL + STAGES;
-  static constexpr int B_KV_EMPTY = B_V_FULL + STAGES;
-  static constexpr int B_S_FULL = B_KV_EMPTY + STAGES;
+  // K and V of a stage are released separately: K once both Q tiles' S MMAs
+  // that read it have completed, V once both P.V MMAs have
+  static constexpr int B_K_EMPTY = B_V_FULL + STAGES;
+  static constexpr int B_V_EMPTY = B_K_EMPTY + STAGES;
+  static constexpr int B_S_FULL = B_V_EMPTY + STAGES;
+  // [2 t + half]: P of keys [64 half, 64 half + 64) of tile t is in TMEM
   static constexpr int B_P_FULL = B_S_FULL + 2;
-  static constexpr int B_O_DONE = B_P_FULL + 2;
+  static constexpr int B_O_DONE = B_P_FULL + 4;
   static constexpr int B_DRAIN = B_O_DONE + 2;  // one per MMA issuer
   static constexpr int B_S_EMPTY = B_DRAIN + 2;  // [tile], early-S schedule only
   static constexpr int B_PV_DONE = B_S_EMPTY + 2;  // [tile], early-S schedule only
-  static constexpr int N_BARS = B_PV_DONE + 2;
+  static constexpr int B_TURN = B_PV_DONE + 2;  // [issuer]: its turn to submit MMAs
+  static constexpr int N_BARS = B_TURN + 2;
   // Early-S schedule (D = 64): P has TMEM columns of its own, so S_t(j+1) is
   // issued as soon as the softmax has read S_t(j) into registers and runs on
   // the tensor core while that softmax computes its exponentials.
@@ -274,9 +281,11 @@ __device__ __forceinline__ void attn_tma_role(const CUtensorMap* tmQ, const CUte
     }
     for (int j = 0; ok && j < it.nkv_max; ++j, ++kv_it) {
       const int s = static_cast<int>(kv_it % L::STAGES);
-      // a stage is free once both MMA issuers released it
+      // a K (V) slot is free once both MMA issuers released it; K slots come
+      // free a whole Q tile step before V slots, so the next K tile lands
+      // well before its S is issued
       if (kv_it >= static_cast<uint32_t>(L::STAGES)) {
-        ok = mbar_wait(&bars[L::B_KV_EMPTY + s], ((kv_it / L::STAGES) - 1u) & 1u, ctl);
+        ok = mbar_wait(&bars[L::B_K_EMPTY + s], ((kv_it / L::STAGES) - 1u) & 1u, ctl);
         if (!ok) break;
       }
       if (static_cast<long long>(kv_it) != p.debug_skip_kv_load) {
@@ -284,6 +293,15 @@ __device__ __forceinline__ void attn_tma_role(const CUtensorMap* tmQ, const CUte
         for (int c = 0; c < L::NCHUNK; ++c)
           attn_load_tile(tmK, smem + L::K_OFF + s * L::TILE_BYTES + c * L::CHUNK_BYTES,
                          &bars[L::B_K_FULL + s], 64 * c, j * ATTN_BLOCK_N, it.kvh, it.b, p.packed);
+      }
+      if (kv_it >= static_cast<uint32_t>(L::STAGES)) {
+        ok = mbar_wait(&bars[L::B_V_EMPTY + s], ((kv_it / L::STAGES) - 1u) & 1u, ctl);
+        if (!ok) {
+          // the K load of this index is in flight but not counted below
+          if (static_cast<long long>(kv_it) != p.debug_skip_kv_load)
+            mbar_wait_drain(&bars[L::B_K_FULL + s], (kv_it / L::STAGES) & 1u, ctl.limit_ns);
+          break;
+        }
       }
       mbar_arrive_expect_tx(&bars[L::B_V_FULL + s], L::TILE_BYTES);
       for (int c = 0; c < L::NCHUNK; ++c)
@@ -307,50 +325,48 @@ __device__ __forceinline__ void attn_tma_role(const CUtensorMap* tmQ, const CUte
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuers: one thread per Q tile
+// MMA issuers: one warp per Q tile, taking turns
 // ---------------------------------------------------------------------------
-// One tcgen05.mma takes a single issuing thread ~100 cycles, more than the
-// 64-cycle tensor time of a 128 x 128 x 16 step, so each Q tile has its own
-// issuer and the two interleave on the tensor core.
-//
-// Issuer t, per KV tile j:  [wait P_t(j)]  O_t += P_t(j) V_j
+// Issuer t, per KV tile j:  [wait P_t(j), keys 0-63]    O_t += P V_j (keys 0-63)
+//                           [wait P_t(j), keys 64-127]  O_t += P V_j (keys 64-127)
 //                           S_t(j+1) = Q_t K_{j+1}^T
-// S_t(j+1) overwrites the TMEM columns that hold P_t(j).  Both MMAs come
-// from the same thread in that order, and the tensor core executes one
+// The softmax hands P over in two halves, so the tensor core multiplies the
+// first 64 keys of P into V while the softmax still computes the second.
+// S_t(j+1) overwrites the TMEM columns that hold P_t(j) (D = 128).  Both MMAs
+// come from the same thread in that order, and the tensor core executes one
 // thread's MMAs in issue order, so P_t(j) has been read before S_t(j+1)
 // writes.  The S_FULL commit after S_t(j+1) fires only when every earlier
 // MMA of the thread, including P_t(j) V_j, has completed, so the softmax may
-// rescale O_t once it sees S_t(j+1).
+// rescale O_t once it sees S_t(j+1).  At D = 64 (early S) P has columns of
+// its own: S_t(j+1) is issued as soon as the softmax has read S_t(j), before
+// P_t(j) V_j, and PV_DONE tells the softmax when P_t(j) V_j has completed.
 //
-// A K/V stage is released when both issuers have arrived: with a commit
-// after their P.V of that KV tile (which follows the S that read its K), or
-// with a plain arrive for a KV tile their Q tile does not need (causal
-// tails), after waiting for the tile to land so that an arrival can never
-// count towards an earlier use of the stage.  O_DONE is signalled only after
-// an item's last P.V, for the epilogue.
-// Bounded poll of a shared flag (set once, never cleared).
-__device__ __forceinline__ bool attn_wait_flag(volatile int* flag, const WaitCtl& c) {
-  const uint64_t t0 = globaltimer_ns();
-  while (*flag == 0) {
-    if (*c.abort_flag) return false;
-    if (globaltimer_ns() - t0 > c.limit_ns) {
-      *c.abort_flag = 1;
-      atomicOr(c.status, c.timeout_code);
-      return false;
-    }
-    __nanosleep(64);
-  }
-  return true;
-}
-
+// Turns (D = 128): the issuers submit their blocks of MMAs (an item's first
+// S, then per KV tile the P.V and next S) strictly in turn, A B A B ..., by
+// passing a token through the TURN barriers.  The tensor core then runs one
+// tile's block to its end before the other's, and each tile's softmax
+// overlaps the other tile's block.  Left to themselves the two issuers'
+// MMAs interleaved on the tensor core: both S tiles completed together and
+// both softmax groups then ran at the same time while the tensor core
+// waited (a clock trace showed ~3,550 cycles per step against 2,048 of
+// tensor work).  An issuer waits for its own operands (P, K, V) before it
+// takes the token, so those waits overlap the other tile's submissions; a
+// block with nothing to compute passes the token on at once.
+//
+// A stage's K and V slots are released separately, each when both issuers
+// have arrived: K with a commit after the issuer's S that read it, V with a
+// commit after its P.V, or, for a KV tile the issuer's Q tile does not need
+// (causal tails), with a plain arrive after waiting for the tile to land, so
+// that an arrival can never count towards an earlier use of the slot.
+// O_DONE is signalled only after an item's last P.V, for the epilogue.
 template <int D>
 __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, uint8_t* smem,
-                                              uint64_t* bars, uint32_t tmem, const WaitCtl& ctl,
-                                              volatile int* tile0_started) {
+                                              uint64_t* bars, uint32_t tmem, const WaitCtl& ctl) {
   // Run by a whole warp: every lane waits and computes the operands, one
   // elected lane issues.  Operands computed by all lanes stay warp-uniform,
   // which keeps the issue of each tcgen05.mma short.
   using L = AttnLayout<D>;
+  constexpr bool TURNS = !L::EARLY_S;
   constexpr uint32_t IDESC_S = idesc_bf16_f32(ATTN_BLOCK_M, ATTN_BLOCK_N, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(ATTN_BLOCK_M, D, true);
   const uint64_t q_desc = smem_desc_sw128(smem_u32(smem + L::Q_OFF) + t * L::TILE_BYTES, 16, 1024);
@@ -362,7 +378,8 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
   constexpr unsigned FULL = 0xffffffffu;
   uint32_t q_uses = 0, p_cnt = 0;
   uint32_t s_issued = 0;  // S MMAs issued (early-S: S_EMPTY phases to wait for)
-  uint32_t kv_it = 0;  // running KV tile index (stage = kv_it % STAGES)
+  uint32_t turns = 0;     // blocks this issuer has submitted (TURNS only)
+  uint32_t kv_it = 0;     // running KV tile index (stage = kv_it % STAGES)
   bool ok = true;
   AttnItem it;
   // S_t = Q_t K^T for the K tile in stage s
@@ -374,18 +391,34 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
       mma_bf16_ss(s_tmem, q_desc + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
     }
   };
+  // the token: tile 0 submits first; each issuer waits for the other's
+  // previous block and hands its own on afterwards
+  bool have_turn = false;
+  auto take_turn = [&]() -> bool {
+    if (!TURNS || have_turn) return true;
+    have_turn = true;
+    if (t == 0 && turns == 0) return true;
+    const uint32_t parity = (t == 0 ? turns - 1u : turns) & 1u;
+    return __all_sync(FULL, mbar_wait(&bars[L::B_TURN + t], parity, ctl));
+  };
+  auto pass_turn = [&]() -> bool {
+    if (!TURNS) return true;
+    bool r = take_turn();  // a block with nothing to compute still waits its turn
+    if (r) {
+      if (elect_one()) mbar_arrive(&bars[L::B_TURN + (1 - t)]);
+      __syncwarp();
+    }
+    ++turns;
+    have_turn = false;
+    return r;
+  };
   for (int k = 0; ok && attn_get_item(p, k, it); ++k) {
     if (t == 0 && it.kv_len_raw != it.kv_len && elect_one())
       atomicOr(p.status, ATTN_STATUS_BAD_KVLEN);
     if (it.nkv_max == 0) continue;
     const int nkv = t ? it.nkv[1] : it.nkv[0];
-    // The two Q tiles' chains (S -> softmax -> P.V) are independent; tile 1
-    // starts half a chain late so that the two softmax groups alternate on
-    // the SM instead of competing.
-    if (t == 1 && k == 0 && it.nkv[0] > 0 && nkv > 0)
-      ok = __all_sync(FULL, attn_wait_flag(tile0_started, ctl));
-    // S_t(0)
-    if (ok) {
+    // S_t(0), or the release of the item's first K tile
+    {
       const int s = static_cast<int>(kv_it % L::STAGES);
       ok = __all_sync(FULL, mbar_wait(&bars[L::B_K_FULL + s], (kv_it / L::STAGES) & 1u, ctl));
       if (ok && nkv > 0) {
@@ -393,76 +426,137 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
         ++q_uses;
         if (L::EARLY_S && ok && s_issued > 0)
           ok = __all_sync(FULL, mbar_wait(&bars[L::B_S_EMPTY + t], (s_issued - 1u) & 1u, ctl));
+        if (ok) ok = take_turn();
         if (ok) {
           tc_fence_after();
           if (elect_one()) {
             issue_s(s);
             mma_commit(&bars[L::B_S_FULL + t]);
+            mma_commit(&bars[L::B_K_EMPTY + s]);
             if (nkv == 1) mma_commit(&bars[L::B_Q_EMPTY + t]);
           }
           __syncwarp();
           ++s_issued;
         }
+      } else if (ok) {
+        if (elect_one()) mbar_arrive(&bars[L::B_K_EMPTY + s]);
+        __syncwarp();
       }
+      if (ok) ok = pass_turn();
     }
     for (int j = 0; ok && j < it.nkv_max; ++j, ++kv_it) {
       const int s = static_cast<int>(kv_it % L::STAGES);
-      if (L::EARLY_S && j + 1 < nkv) {
-        // S_t(j+1) as soon as the softmax has read S_t(j) into registers: it
-        // runs on the tensor core while that softmax computes P_t(j)
-        const uint32_t kv = kv_it + 1u;
-        const int s1 = static_cast<int>(kv % L::STAGES);
-        ok = __all_sync(FULL, mbar_wait(&bars[L::B_S_EMPTY + t], (s_issued - 1u) & 1u, ctl));
-        if (!ok) break;
-        ok = __all_sync(FULL, mbar_wait(&bars[L::B_K_FULL + s1], (kv / L::STAGES) & 1u, ctl));
-        if (!ok) break;
-        tc_fence_after();
-        if (elect_one()) {
-          issue_s(s1);
-          mma_commit(&bars[L::B_S_FULL + t]);
-          if (j + 2 == nkv) mma_commit(&bars[L::B_Q_EMPTY + t]);
-        }
-        __syncwarp();
-        ++s_issued;
-      }
-      ok = __all_sync(FULL, mbar_wait(&bars[L::B_V_FULL + s], (kv_it / L::STAGES) & 1u, ctl));
-      if (!ok) break;
-      if (j < nkv) {
-        // O_t += P_t(j) V_j
-        ok = __all_sync(FULL, mbar_wait(&bars[L::B_P_FULL + t], p_cnt & 1u, ctl));
-        if (!ok) break;
-        ++p_cnt;
-        tc_fence_after();
-        const uint64_t vd = v_desc + static_cast<uint64_t>((s * L::TILE_BYTES) >> 4);
-        if (elect_one()) {
+      const uint32_t kv1 = kv_it + 1u;
+      const int s1 = static_cast<int>(kv1 % L::STAGES);
+      const uint64_t vd = v_desc + static_cast<uint64_t>((s * L::TILE_BYTES) >> 4);
+      // O_t += P_t(j) V_j for the keys of one half of P
+      auto issue_pv = [&](int half) {
 #pragma unroll
-          for (int kk = 0; kk < ATTN_BLOCK_N / 16; ++kk)
-            mma_bf16_ts(o_tmem, p_tmem + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4),
-                        IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
-          // K_j (read by S_t(j), issued earlier) and V_j are free once this
-          // P.V completes; O_t is final after the item's last P.V
-          mma_commit(&bars[L::B_KV_EMPTY + s]);
-          if (L::EARLY_S) mma_commit(&bars[L::B_PV_DONE + t]);
-          if (j == nkv - 1) mma_commit(&bars[L::B_O_DONE + t]);
-        }
-        __syncwarp();
-      } else {
-        if (elect_one()) mbar_arrive(&bars[L::B_KV_EMPTY + s]);
-        __syncwarp();
-      }
-      if (!L::EARLY_S && j + 1 < it.nkv_max) {
-        const int s1 = static_cast<int>((kv_it + 1) % L::STAGES);
-        ok = __all_sync(FULL,
-                        mbar_wait(&bars[L::B_K_FULL + s1], ((kv_it + 1) / L::STAGES) & 1u, ctl));
-        if (!ok) break;
+        for (int kk = 4 * half; kk < 4 * half + 4; ++kk)
+          mma_bf16_ts(o_tmem, p_tmem + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4),
+                      IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+      };
+      if constexpr (L::EARLY_S) {
         if (j + 1 < nkv) {
-          // S_t(j+1) = Q_t K_{j+1}^T
+          // S_t(j+1) as soon as the softmax has read S_t(j) into registers:
+          // it runs on the tensor core while that softmax computes P_t(j)
+          ok = __all_sync(FULL, mbar_wait(&bars[L::B_S_EMPTY + t], (s_issued - 1u) & 1u, ctl));
+          if (!ok) break;
+          ok = __all_sync(FULL, mbar_wait(&bars[L::B_K_FULL + s1], (kv1 / L::STAGES) & 1u, ctl));
+          if (!ok) break;
+          tc_fence_after();
           if (elect_one()) {
             issue_s(s1);
             mma_commit(&bars[L::B_S_FULL + t]);
+            mma_commit(&bars[L::B_K_EMPTY + s1]);
             if (j + 2 == nkv) mma_commit(&bars[L::B_Q_EMPTY + t]);
           }
           __syncwarp();
+          ++s_issued;
+        }
+        ok = __all_sync(FULL, mbar_wait(&bars[L::B_V_FULL + s], (kv_it / L::STAGES) & 1u, ctl));
+        if (!ok) break;
+        if (j < nkv) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            ok = __all_sync(FULL, mbar_wait(&bars[L::B_P_FULL + 2 * t + half], p_cnt & 1u, ctl));
+            if (!ok) break;
+            tc_fence_after();
+            if (elect_one()) {
+              issue_pv(half);
+              if (half == 1) {
+                // V_j is free once this P.V completes; O_t is final after
+                // the item's last P.V
+                mma_commit(&bars[L::B_V_EMPTY + s]);
+                mma_commit(&bars[L::B_PV_DONE + t]);
+                if (j == nkv - 1) mma_commit(&bars[L::B_O_DONE + t]);
+              }
+            }
+            __syncwarp();
+          }
+          if (!ok) break;
+          ++p_cnt;
+        } else {
+          if (elect_one()) mbar_arrive(&bars[L::B_V_EMPTY + s]);
+          __syncwarp();
+        }
+        if (j + 1 < it.nkv_max && j + 1 >= nkv) {
+          // this Q tile needs no more keys of the item: release the K tile
+          ok = __all_sync(FULL, mbar_wait(&bars[L::B_K_FULL + s1], (kv1 / L::STAGES) & 1u, ctl));
+          if (!ok) break;
+          if (elect_one()) mbar_arrive(&bars[L::B_K_EMPTY + s1]);
+          __syncwarp();
+        }
+      } else {
+        // every operand of the block is waited for before the turn is taken,
+        // so that the block's MMAs then go out back to back
+        const bool has_k1 = j + 1 < it.nkv_max;
+        ok = __all_sync(FULL, mbar_wait(&bars[L::B_V_FULL + s], (kv_it / L::STAGES) & 1u, ctl));
+        if (ok && has_k1)
+          ok = __all_sync(FULL, mbar_wait(&bars[L::B_K_FULL + s1], (kv1 / L::STAGES) & 1u, ctl));
+        if (!ok) break;
+        if (j < nkv) {
+          const bool s_next = j + 1 < nkv;
+          ok = __all_sync(FULL, mbar_wait(&bars[L::B_P_FULL + 2 * t], p_cnt & 1u, ctl));
+          if (ok) ok = take_turn();
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) issue_pv(0);
+          __syncwarp();
+          ok = __all_sync(FULL, mbar_wait(&bars[L::B_P_FULL + 2 * t + 1], p_cnt & 1u, ctl));
+          if (!ok) break;
+          ++p_cnt;
+          tc_fence_after();
+          if (elect_one()) {
+            issue_pv(1);
+            // S_t(j+1) = Q_t K_{j+1}^T, after P_t(j) V_j
+            if (s_next) issue_s(s1);
+          }
+          __syncwarp();
+          ok = pass_turn();  // the other tile's block may follow on the tensor core
+          if (elect_one()) {
+            // V_j is free once this P.V completes, K_{j+1} once S_t(j+1) has;
+            // O_t is final after the item's last P.V
+            mma_commit(&bars[L::B_V_EMPTY + s]);
+            if (j == nkv - 1) mma_commit(&bars[L::B_O_DONE + t]);
+            if (s_next) {
+              mma_commit(&bars[L::B_S_FULL + t]);
+              mma_commit(&bars[L::B_K_EMPTY + s1]);
+              if (j + 2 == nkv) mma_commit(&bars[L::B_Q_EMPTY + t]);
+            } else if (has_k1) {
+              mbar_arrive(&bars[L::B_K_EMPTY + s1]);
+            }
+          }
+          __syncwarp();
+          if (s_next) ++s_issued;
+        } else {
+          // nothing to compute for this Q tile: release V_j and K_{j+1}
+          if (elect_one()) {
+            mbar_arrive(&bars[L::B_V_EMPTY + s]);
+            if (has_k1) mbar_arrive(&bars[L::B_K_EMPTY + s1]);
+          }
+          __syncwarp();
+          ok = pass_turn();
         }
       }
     }
@@ -479,7 +573,7 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
 template <int D>
 __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams& p,
                                                   uint64_t* bars, uint32_t tmem,
-                                                  const WaitCtl& ctl, volatile int* tile0_started) {
+                                                  const WaitCtl& ctl) {
   using L = AttnLayout<D>;
   const int rloc = static_cast<int>(threadIdx.x & 127u);
   const uint32_t lane_base = static_cast<uint32_t>(threadIdx.x & 96u) << 16;
@@ -617,6 +711,11 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
           lb_d = add_bf16hi_f32(lb_d, pk[i + 1]);
         }
         tmem_st_32x32b_x32(p_tmem + 32u * half, pk);
+        // each half goes to the MMA issuer as soon as it is in TMEM: the
+        // tensor core multiplies it into V while the other half is computed
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[L::B_P_FULL + 2 * t + half]);
       }
       {
         float x0, x1;
@@ -624,10 +723,6 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
         l += x0 + x1;
         lb += (lb_a + lb_b) + (lb_c + lb_d);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars[L::B_P_FULL + t]);
-      if (t == 0 && k == 0 && j == 0 && threadIdx.x == 0) *tile0_started = 1;
     }
     if (!ok) break;
     // epilogue: O / lb (bf16), LSE; padded and empty rows are exactly 0 / -inf
@@ -694,17 +789,16 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
-  volatile int* tile0_started = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 8);
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31u);
 
   if (threadIdx.x == 0) {
-    *tile0_started = 0;
     for (int t = 0; t < ATTN_QTILES; ++t) {
       mbar_init(&bars[L::B_Q_FULL + t], 1);
       mbar_init(&bars[L::B_Q_EMPTY + t], 1);
       mbar_init(&bars[L::B_S_FULL + t], 1);
-      mbar_init(&bars[L::B_P_FULL + t], 128);
+      mbar_init(&bars[L::B_P_FULL + 2 * t], 128);
+      mbar_init(&bars[L::B_P_FULL + 2 * t + 1], 128);
       mbar_init(&bars[L::B_O_DONE + t], 1);
       mbar_init(&bars[L::B_S_EMPTY + t], 128);
       mbar_init(&bars[L::B_PV_DONE + t], 1);
@@ -712,10 +806,13 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(&bars[L::B_K_FULL + s], 1);
       mbar_init(&bars[L::B_V_FULL + s], 1);
-      mbar_init(&bars[L::B_KV_EMPTY + s], ATTN_QTILES);  // one arrival per MMA issuer
+      mbar_init(&bars[L::B_K_EMPTY + s], ATTN_QTILES);  // one arrival per MMA issuer
+      mbar_init(&bars[L::B_V_EMPTY + s], ATTN_QTILES);
     }
-    mbar_init(&bars[L::B_DRAIN + 0], 1);
-    mbar_init(&bars[L::B_DRAIN + 1], 1);
+    for (int t = 0; t < ATTN_QTILES; ++t) {
+      mbar_init(&bars[L::B_DRAIN + t], 1);
+      mbar_init(&bars[L::B_TURN + t], 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -743,11 +840,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     if (warp == 9) {
       if (lane == 0) attn_tma_role<D>(&tmQ, &tmK, &tmV, p, smem, bars, ctl);
     } else if (warp == 8 || warp == 10) {
-      attn_mma_role<D>(warp == 8 ? 0 : 1, p, smem, bars, tmem, ctl, tile0_started);
+      attn_mma_role<D>(warp == 8 ? 0 : 1, p, smem, bars, tmem, ctl);
     }
   } else {
     reg_alloc<ATTN_REGS_SOFTMAX>();
-    attn_softmax_role<D>(warp >> 2, p, bars, tmem, ctl, tile0_started);
+    attn_softmax_role<D>(warp >> 2, p, bars, tmem, ctl);
   }
 
   tc_fence_before();
