@@ -533,14 +533,17 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
             if (s_next) issue_s(s1);
           }
           __syncwarp();
-          ok = pass_turn();  // the other tile's block may follow on the tensor core
+          // the other tile's block may follow on the tensor core (handing the
+          // token on earlier, or through a spin on a shared word instead of
+          // an mbarrier, measured no faster)
+          ok = pass_turn();
           if (elect_one()) {
+            if (s_next) mma_commit(&bars[L::B_S_FULL + t]);
             // V_j is free once this P.V completes, K_{j+1} once S_t(j+1) has;
             // O_t is final after the item's last P.V
             mma_commit(&bars[L::B_V_EMPTY + s]);
             if (j == nkv - 1) mma_commit(&bars[L::B_O_DONE + t]);
             if (s_next) {
-              mma_commit(&bars[L::B_S_FULL + t]);
               mma_commit(&bars[L::B_K_EMPTY + s1]);
               if (j + 2 == nkv) mma_commit(&bars[L::B_Q_EMPTY + t]);
             } else if (has_k1) {

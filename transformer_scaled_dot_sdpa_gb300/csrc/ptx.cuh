@@ -56,15 +56,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// The value itself, hidden from the compiler's loop-invariant code motion:
-// an operand recomputed from it at its use costs a few instructions there
-// instead of a register held across the loop.
-__device__ __forceinline__ uint32_t opaque_u32(uint32_t x) {
-  uint32_t y;
-  asm volatile("mov.b32 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
