@@ -23,15 +23,12 @@
 //                    per-warpgroup register reallocation needs)
 // TMEM (512 columns x 128 lanes, fp32):
 //   [  0,128) S of tile 0, [128,256) S of tile 1
-//   D = 128: P (bf16 pairs) reuses the high 64 columns of its S;
-//            [256,384) O accumulator of tile 0, [384,512) O of tile 1
-//   D = 64:  [256,320) O of tile 0, [320,384) O of tile 1, and P has columns
-//            of its own: [384,448) P of tile 0, [448,512) P of tile 1
+//   P (bf16 pairs) reuses the high 64 columns of its S;
+//   [256,384) O accumulator of tile 0, [384,512) O of tile 1 (D = 64: the
+//   first 80 columns of each, column 64 holding the row sum of P)
 // Each Q tile has its own MMA issuer, and at D = 128 the two take turns: while
 // one softmax group works on its S, the tensor core runs the other tile's P.V
-// and next S.  At D = 64 the
-// separate P columns also let S_t(j+1) start as soon as the softmax has read
-// S_t(j) ("early S"), so it overlaps that softmax's exponentials.
+// and next S.
 //
 // Softmax state per row (one thread per row = one TMEM lane): m in log2
 // units (already multiplied by scale*log2 e) and two running sums: l of the
@@ -130,7 +127,17 @@ struct AttnLayout {
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + ATTN_QTILES * TILE_BYTES;
   static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
-  static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
+  // Row sum on the tensor core (D = 64): the P.V MMA runs with N = D + 16,
+  // its B operand's second 64-column atom a constant tile of ones (ONES_OFF,
+  // reached from each V stage through the descriptor's leading-byte offset),
+  // so O column D accumulates the sum of the bf16 P that the MMA multiplies
+  // into V.  The softmax then keeps only the fp32 sum for the LSE.  At
+  // D = 128 the two O accumulators leave no TMEM columns for it.
+  static constexpr bool TC_ROWSUM = (D == 64);
+  static constexpr int O_N = TC_ROWSUM ? D + 16 : D;  // N of the P.V MMA
+  static constexpr int ONES_OFF = V_OFF + STAGES * TILE_BYTES;
+  static constexpr int ONES_BYTES = TC_ROWSUM ? CHUNK_BYTES : 0;
+  static constexpr int BAR_OFF = ONES_OFF + ONES_BYTES;
   // barrier indices
   static constexpr int B_Q_FULL = 0;
   static constexpr int B_Q_EMPTY = 2;
@@ -145,19 +152,14 @@ struct AttnLayout {
   static constexpr int B_P_FULL = B_S_FULL + 2;
   static constexpr int B_O_DONE = B_P_FULL + 4;
   static constexpr int B_DRAIN = B_O_DONE + 2;  // one per MMA issuer
-  static constexpr int B_S_EMPTY = B_DRAIN + 2;  // [tile], early-S schedule only
-  static constexpr int B_PV_DONE = B_S_EMPTY + 2;  // [tile], early-S schedule only
-  static constexpr int B_TURN = B_PV_DONE + 2;  // [issuer]: its turn to submit MMAs
+  static constexpr int B_TURN = B_DRAIN + 2;  // [issuer]: its turn to submit MMAs
   static constexpr int N_BARS = B_TURN + 2;
-  // Early-S schedule (D = 64): P has TMEM columns of its own, so S_t(j+1) is
-  // issued as soon as the softmax has read S_t(j) into registers and runs on
-  // the tensor core while that softmax computes its exponentials.
-  static constexpr bool EARLY_S = (D == 64);
-  // TMEM columns of tile t: S at 128 t; O at 256 + O_STRIDE t; P (bf16
-  // pairs) at p_col(t): the high half of S_t, or its own 64 columns
-  static constexpr uint32_t O_STRIDE = EARLY_S ? 64u : 128u;
+  // TMEM columns of tile t: S at 128 t; O at 256 + 128 t (D, or D + 16
+  // with the row sum, of them used); P (bf16 pairs) in the high 64 columns
+  // of S_t, which the softmax has read before it writes P
+  static constexpr uint32_t O_STRIDE = 128u;
   static __device__ __forceinline__ uint32_t p_col(int t) {
-    return EARLY_S ? 384u + 64u * static_cast<uint32_t>(t) : 128u * static_cast<uint32_t>(t) + 64u;
+    return 128u * static_cast<uint32_t>(t) + 64u;
   }
   static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
@@ -332,14 +334,12 @@ __device__ __forceinline__ void attn_tma_role(const CUtensorMap* tmQ, const CUte
 //                           S_t(j+1) = Q_t K_{j+1}^T
 // The softmax hands P over in two halves, so the tensor core multiplies the
 // first 64 keys of P into V while the softmax still computes the second.
-// S_t(j+1) overwrites the TMEM columns that hold P_t(j) (D = 128).  Both MMAs
+// S_t(j+1) overwrites the TMEM columns that hold P_t(j).  Both MMAs
 // come from the same thread in that order, and the tensor core executes one
 // thread's MMAs in issue order, so P_t(j) has been read before S_t(j+1)
 // writes.  The S_FULL commit after S_t(j+1) fires only when every earlier
 // MMA of the thread, including P_t(j) V_j, has completed, so the softmax may
-// rescale O_t once it sees S_t(j+1).  At D = 64 (early S) P has columns of
-// its own: S_t(j+1) is issued as soon as the softmax has read S_t(j), before
-// P_t(j) V_j, and PV_DONE tells the softmax when P_t(j) V_j has completed.
+// rescale O_t once it sees S_t(j+1).
 //
 // Turns (D = 128): the issuers submit their blocks of MMAs (an item's first
 // S, then per KV tile the P.V and next S) strictly in turn, A B A B ..., by
@@ -366,9 +366,11 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
   // elected lane issues.  Operands computed by all lanes stay warp-uniform,
   // which keeps the issue of each tcgen05.mma short.
   using L = AttnLayout<D>;
-  constexpr bool TURNS = !L::EARLY_S;
+  // (turns at D = 128 only: at D = 64 a tile's MMAs take a fraction of its
+  // softmax, and the two softmax groups run better side by side)
+  constexpr bool TURNS = (D == 128);
   constexpr uint32_t IDESC_S = idesc_bf16_f32(ATTN_BLOCK_M, ATTN_BLOCK_N, false);
-  constexpr uint32_t IDESC_O = idesc_bf16_f32(ATTN_BLOCK_M, D, true);
+  constexpr uint32_t IDESC_O = idesc_bf16_f32(ATTN_BLOCK_M, L::O_N, true);
   const uint64_t q_desc = smem_desc_sw128(smem_u32(smem + L::Q_OFF) + t * L::TILE_BYTES, 16, 1024);
   const uint64_t k_desc = smem_desc_sw128(smem_u32(smem + L::K_OFF), 16, 1024);
   const uint64_t v_desc = smem_desc_sw128(smem_u32(smem + L::V_OFF), L::CHUNK_BYTES, 1024);
@@ -377,7 +379,6 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
   const uint32_t o_tmem = tmem + 256u + static_cast<uint32_t>(t) * L::O_STRIDE;
   constexpr unsigned FULL = 0xffffffffu;
   uint32_t q_uses = 0, p_cnt = 0;
-  uint32_t s_issued = 0;  // S MMAs issued (early-S: S_EMPTY phases to wait for)
   uint32_t turns = 0;     // blocks this issuer has submitted (TURNS only)
   uint32_t kv_it = 0;     // running KV tile index (stage = kv_it % STAGES)
   bool ok = true;
@@ -424,8 +425,6 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
       if (ok && nkv > 0) {
         ok = __all_sync(FULL, mbar_wait(&bars[L::B_Q_FULL + t], q_uses & 1u, ctl));
         ++q_uses;
-        if (L::EARLY_S && ok && s_issued > 0)
-          ok = __all_sync(FULL, mbar_wait(&bars[L::B_S_EMPTY + t], (s_issued - 1u) & 1u, ctl));
         if (ok) ok = take_turn();
         if (ok) {
           tc_fence_after();
@@ -436,7 +435,6 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
             if (nkv == 1) mma_commit(&bars[L::B_Q_EMPTY + t]);
           }
           __syncwarp();
-          ++s_issued;
         }
       } else if (ok) {
         if (elect_one()) mbar_arrive(&bars[L::B_K_EMPTY + s]);
@@ -448,7 +446,13 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
       const int s = static_cast<int>(kv_it % L::STAGES);
       const uint32_t kv1 = kv_it + 1u;
       const int s1 = static_cast<int>(kv1 % L::STAGES);
-      const uint64_t vd = v_desc + static_cast<uint64_t>((s * L::TILE_BYTES) >> 4);
+      // V of stage s; with the row sum its second N atom is the ones tile
+      const uint64_t vd =
+          L::TC_ROWSUM
+              ? smem_desc_sw128(smem_u32(smem + L::V_OFF) + s * L::TILE_BYTES,
+                                static_cast<uint32_t>(L::ONES_OFF - L::V_OFF - s * L::TILE_BYTES),
+                                1024)
+              : v_desc + static_cast<uint64_t>((s * L::TILE_BYTES) >> 4);
       // O_t += P_t(j) V_j for the keys of one half of P
       auto issue_pv = [&](int half) {
 #pragma unroll
@@ -456,58 +460,7 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
           mma_bf16_ts(o_tmem, p_tmem + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4),
                       IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
       };
-      if constexpr (L::EARLY_S) {
-        if (j + 1 < nkv) {
-          // S_t(j+1) as soon as the softmax has read S_t(j) into registers:
-          // it runs on the tensor core while that softmax computes P_t(j)
-          ok = __all_sync(FULL, mbar_wait(&bars[L::B_S_EMPTY + t], (s_issued - 1u) & 1u, ctl));
-          if (!ok) break;
-          ok = __all_sync(FULL, mbar_wait(&bars[L::B_K_FULL + s1], (kv1 / L::STAGES) & 1u, ctl));
-          if (!ok) break;
-          tc_fence_after();
-          if (elect_one()) {
-            issue_s(s1);
-            mma_commit(&bars[L::B_S_FULL + t]);
-            mma_commit(&bars[L::B_K_EMPTY + s1]);
-            if (j + 2 == nkv) mma_commit(&bars[L::B_Q_EMPTY + t]);
-          }
-          __syncwarp();
-          ++s_issued;
-        }
-        ok = __all_sync(FULL, mbar_wait(&bars[L::B_V_FULL + s], (kv_it / L::STAGES) & 1u, ctl));
-        if (!ok) break;
-        if (j < nkv) {
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            ok = __all_sync(FULL, mbar_wait(&bars[L::B_P_FULL + 2 * t + half], p_cnt & 1u, ctl));
-            if (!ok) break;
-            tc_fence_after();
-            if (elect_one()) {
-              issue_pv(half);
-              if (half == 1) {
-                // V_j is free once this P.V completes; O_t is final after
-                // the item's last P.V
-                mma_commit(&bars[L::B_V_EMPTY + s]);
-                mma_commit(&bars[L::B_PV_DONE + t]);
-                if (j == nkv - 1) mma_commit(&bars[L::B_O_DONE + t]);
-              }
-            }
-            __syncwarp();
-          }
-          if (!ok) break;
-          ++p_cnt;
-        } else {
-          if (elect_one()) mbar_arrive(&bars[L::B_V_EMPTY + s]);
-          __syncwarp();
-        }
-        if (j + 1 < it.nkv_max && j + 1 >= nkv) {
-          // this Q tile needs no more keys of the item: release the K tile
-          ok = __all_sync(FULL, mbar_wait(&bars[L::B_K_FULL + s1], (kv1 / L::STAGES) & 1u, ctl));
-          if (!ok) break;
-          if (elect_one()) mbar_arrive(&bars[L::B_K_EMPTY + s1]);
-          __syncwarp();
-        }
-      } else {
+      {
         // every operand of the block is waited for before the turn is taken,
         // so that the block's MMAs then go out back to back
         const bool has_k1 = j + 1 < it.nkv_max;
@@ -551,7 +504,6 @@ __device__ __forceinline__ void attn_mma_role(const int t, const AttnParams& p, 
             }
           }
           __syncwarp();
-          if (s_next) ++s_issued;
         } else {
           // nothing to compute for this Q tile: release V_j and K_{j+1}
           if (elect_one()) {
@@ -612,11 +564,6 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
       reg_fence(rb);
       reg_fence(rc);
       reg_fence(rd);
-      if constexpr (L::EARLY_S) {
-        // S_t(j) is in registers: its columns may take S_t(j+1)
-        tc_fence_before();
-        mbar_arrive(&bars[L::B_S_EMPTY + t]);
-      }
       float s[128];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -644,26 +591,16 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
       const float m_tile = mx * c;  // scale > 0, so the max commutes with it
       const float m_new = fmaxf(m, m_tile);
       const bool need = m_new > m + ATTN_RESCALE_THRESHOLD;
-      if (L::EARLY_S && j > 0) {
-        // S_t(j) was issued before P_t(j-1) V, so its commit does not cover
-        // that MMA: wait for it before O is rescaled or P_t(j) overwrites
-        // the P columns it reads
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(&bars[L::B_PV_DONE + t], (s_cnt - 2u) & 1u, ctl));
-        if (!ok) break;
-        tc_fence_after();
-      }
       if (__any_sync(0xffffffffu, need && j > 0)) {
         // rescale this row's O accumulator.  P_t(j-1) V has completed: the
-        // commit that signalled S_t(j) covers every earlier MMA of the issuer
-        // (early-S: the wait above).
+        // commit that signalled S_t(j) covers every earlier MMA of the issuer.
         const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
         const uint64_t a2 = f2_pack(alpha, alpha);
         // a rolled loop: the rescale is rare, and the softmax loop's code
         // stays small (bit-identical; unrolled it cost 1-6% at d = 128 in
         // instruction fetch)
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < (L::O_N + 31) / 32; ++cc) {
           uint32_t ro[32];
           tmem_ld_32x32b_x32(o_tmem + cc * 32u, ro);
           tmem_ld_wait(ro);
@@ -708,10 +645,12 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
           pk[i + 1] = pack_bf16x2(p2, p3);
           lf_a = f2_add(lf_a, f2_pack(p0, p1));
           lf_b = f2_add(lf_b, f2_pack(p2, p3));
-          lb_a = add_bf16lo_f32(lb_a, pk[i]);
-          lb_b = add_bf16hi_f32(lb_b, pk[i]);
-          lb_c = add_bf16lo_f32(lb_c, pk[i + 1]);
-          lb_d = add_bf16hi_f32(lb_d, pk[i + 1]);
+          if constexpr (!L::TC_ROWSUM) {
+            lb_a = add_bf16lo_f32(lb_a, pk[i]);
+            lb_b = add_bf16hi_f32(lb_b, pk[i]);
+            lb_c = add_bf16lo_f32(lb_c, pk[i + 1]);
+            lb_d = add_bf16hi_f32(lb_d, pk[i + 1]);
+          }
         }
         tmem_st_32x32b_x32(p_tmem + 32u * half, pk);
         // each half goes to the MMA issuer as soon as it is in TMEM: the
@@ -735,6 +674,16 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
+    }
+    if constexpr (L::TC_ROWSUM) {
+      // the sum of the bf16 P, from column D of the accumulator
+      lb = 0.f;
+      if (nkv > 0) {
+        uint32_t rs[32];
+        tmem_ld_32x32b_x32(o_tmem + static_cast<uint32_t>(D), rs);
+        tmem_ld_wait(rs);
+        lb = __uint_as_float(rs[0]);
+      }
     }
     const bool in_range = r < p.Lq;
     const bool zero_row = padded_row || nkv == 0 || limit <= 0 || !(lb > 0.f);
@@ -803,8 +752,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       mbar_init(&bars[L::B_P_FULL + 2 * t], 128);
       mbar_init(&bars[L::B_P_FULL + 2 * t + 1], 128);
       mbar_init(&bars[L::B_O_DONE + t], 1);
-      mbar_init(&bars[L::B_S_EMPTY + t], 128);
-      mbar_init(&bars[L::B_PV_DONE + t], 1);
     }
     for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(&bars[L::B_K_FULL + s], 1);
@@ -818,6 +765,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     }
     *abort_flag = 0;
     fence_mbar_init();
+  }
+  if constexpr (L::TC_ROWSUM) {
+    // the ones operand of the row sum: bf16 1.0 everywhere (so its swizzle
+    // does not matter), written once and read by the tensor core
+    uint4* ones = reinterpret_cast<uint4*>(smem + L::ONES_OFF);
+    for (int i = static_cast<int>(threadIdx.x); i < L::ONES_BYTES / 16; i += ATTN_THREADS)
+      ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
   }
   if (warp == 8) {
     tmem_alloc(tmem_slot, ATTN_TMEM_COLS);
