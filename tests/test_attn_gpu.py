@@ -244,6 +244,24 @@ def test_long_context_two_whole_heads(cuda_lib):
 
 MASK_BR = 4  # causal, aligned to the last key
 
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mask", [MASK_CAUSAL, MASK_CAUSAL | MASK_PADDING, MASK_BR | MASK_PADDING],
+                         ids=["causal", "causal+pad", "br+pad"])
+def test_many_items_per_cta_with_empty_tiles(cuda_lib, d, mask):
+    """192 heads of 300 rows: more 256-row items than SMs, so each CTA runs
+    several items in turn, and in every second one (rows 256-511) the second
+    Q tile lies past the sequence and has nothing to compute while the first
+    does.  With padding the lengths also leave whole tiles empty.  Every row
+    against the oracle."""
+    B, H, L = 2, 96, 300
+    inp = make_attention_inputs(B, H, L, L, d, d, seed=31 + d + mask)
+    inp["kv_lens"] = _kv_lens(B, L, seed=37 + mask, special=[140, 300])
+    O, Lse = _run(cuda_lib, inp, mask)
+    Or, Lr = oracle.attention(inp["q"], inp["k"], inp["v"], mask_kind=mask,
+                              kv_lens=inp["kv_lens"] if mask & MASK_PADDING else None)
+    compare_attention(O, Lse, Or, Lr, "B%d h%d L%d d%d mask %d" % (B, H, L, d, mask))
+
 GQA = [(2, 8, 8, 300, 300, 128), (1, 8, 2, 257, 257, 64), (2, 6, 1, 200, 200, 128),
        (1, 16, 4, 1000, 1000, 128), (1, 8, 4, 64, 900, 64)]
 
