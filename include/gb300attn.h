@@ -408,7 +408,8 @@ void attn_set_wait_limit_ns(uint64_t ns);
  * in how a CTA's work is laid out on the SM:
  *   ATTN_SCHEDULE_TWO_QTILES  256 query rows per work item, two 128-row Q
  *                             tiles with one softmax warpgroup and one MMA
- *                             issuer warp each
+ *                             issuer warp each (at d = 128 the two issuers
+ *                             submit their MMAs to the tensor core in turn)
  *   ATTN_SCHEDULE_SPLIT_KEYS  128 query rows per work item, its key tiles
  *                             dealt alternately to two softmax warpgroups
  *                             with separate accumulators, merged at the end
