@@ -555,9 +555,19 @@ class LayerRun:
                                                out=oh, return_lse=False, stream=stream),
                             steps, stream, dev, flush)
         g.check_device_status(stream)
+        # the two projections through torch.matmul (cuBLAS), timed the same
+        # way, for comparison only
+        with torch.cuda.stream(stream):
+            torch.matmul(x2, self.wqkv, out=qkv)
+            torch.matmul(cat, self.wo, out=self.y.view(N, dm))
+            mm_qkv = time_calls(lambda: torch.matmul(x2, self.wqkv, out=qkv), steps, stream, dev,
+                                flush)
+            mm_wo = time_calls(lambda: torch.matmul(cat, self.wo, out=self.y.view(N, dm)), steps,
+                               stream, dev, flush)
         return {"ms": ms, "ms_max": max_over_ranks(ms, world), "flushed": flush is not None,
                 "clocks": clk, "stage_ms": {"qkv_gemm": ms_qkv, "attention": ms_att,
-                                            "wo_gemm": ms_wo}}
+                                            "wo_gemm": ms_wo},
+                "torch_matmul_ms": {"qkv_gemm": mm_qkv, "wo_gemm": mm_wo}}
 
 
 def layer_record(run, t, world, steps):
@@ -583,7 +593,9 @@ def layer_record(run, t, world, steps):
                 "stages_ms": {k: v[1] for k, v in stages.items()},
                 "stages_tflops": {k: v[0] / (v[1] * 1e-3) / 1e12 for k, v in stages.items()},
                 "stages_frac": {k: v[0] / (v[1] * 1e-3) / 1e12 / peaks["bf16_tflops"]
-                                for k, v in stages.items()}}
+                                for k, v in stages.items()},
+                "torch_matmul_tflops": {k: stages[k][0] / (ms * 1e-3) / 1e12
+                                        for k, ms in t.get("torch_matmul_ms", {}).items()}}
     cfg = {"workload": w.name, "B": w.B, "L": w.L, "d_model": dm, "H": w.H,
            "mask": "causal" if w.mask_kind & MASK_CAUSAL else "none",
            "parallelism": "replicas x%d" % world,
