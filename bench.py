@@ -38,9 +38,9 @@ from sdpa_workloads import (BENCH_WORKLOAD, MASK_CAUSAL, MASK_CAUSAL_BOTTOM_RIGH
 METRIC = "attention fwd TFLOP/s on 1 GB300 and % of roofline (tensor/exp/HBM bound)"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# sources whose hash a committed DRAM-traffic figure is tied to, per kernel
 E2E_WINDOWS = 3  # end-to-end timing windows; the median one is reported
 
+# sources whose hash a committed DRAM-traffic figure is tied to, per kernel
 KERNEL_SOURCES = {
     "attn_fwd_kernel": ["attn_fwd_kernel.cuh", "ptx.cuh"],
     "gemm_bf16_kernel": ["gemm_kernel.cuh", "ptx.cuh"],

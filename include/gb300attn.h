@@ -362,7 +362,8 @@ attn_status_t mha_layer_fwd_noalloc(const void* X, const void* W_QKV, const void
  * output: the projection step of the layer, exposed for direct use.
  *   A bf16 [M, K], B bf16 [K, N], C bf16 [M, N], all row-major.
  * Supported: M multiple of 128, N multiple of 256, K multiple of 64;
- * pointers 16-byte aligned.
+ * pointers 16-byte aligned.  A 32-byte aligned C is written in whole 32-byte
+ * sectors (faster); a C aligned to 16 bytes only, in 16-byte pieces.
  */
 attn_status_t attn_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K,
                              void* stream);

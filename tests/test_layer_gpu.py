@@ -43,6 +43,24 @@ def test_gemm_matches_fp64_matmul(cuda_lib, M, N, K):
     assert np.all(err <= bound), "max excess %.3g" % (err - bound).max()
 
 
+@pytest.mark.parametrize("M,N,K", [(640, 512, 128), (2176, 1024, 128)])
+def test_gemm_c_aligned_to_16_bytes_only(cuda_lib, M, N, K):
+    """A C that is 16- but not 32-byte aligned is written in 16-byte pieces
+    instead of whole sectors: the same values as into an aligned C, and
+    nothing written outside C."""
+    import torch
+    a, b = _gemm_case(M, N, K, seed=7 * M + N)
+    A, Bm = up(a), up(b)
+    C_al = cuda_lib.gemm_bf16(A, Bm)
+    buf = torch.full((M * N + 32,), float("nan"), dtype=torch.bfloat16, device=A.device)
+    assert buf.data_ptr() % 32 == 0
+    C_16 = buf[8:8 + M * N].view(M, N)  # 16 bytes past a 32-byte boundary
+    cuda_lib.gemm_bf16(A, Bm, out=C_16)
+    cuda_lib.check_device_status()
+    assert torch.equal(C_16, C_al)
+    assert torch.isnan(buf[:8]).all() and torch.isnan(buf[8 + M * N:]).all()
+
+
 def _layer_run(g, inp, H, mask, kv=None):
     import torch
     kvt = torch.from_numpy(kv).cuda() if kv is not None else None

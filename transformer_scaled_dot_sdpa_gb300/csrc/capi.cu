@@ -302,11 +302,10 @@ attn_status_t map_2d(CUtensorMap* m, const void* base, int rows, int cols, int c
 // C[M,N] = A[M,K] B[K,N]; sizes already validated.
 attn_status_t run_gemm(DeviceState* ds, const void* A, const void* Bm, void* C, int M, int N,
                        int K, cudaStream_t stream, bool dependent = false) {
-  CUtensorMap ma, mb, mc;
+  CUtensorMap ma, mb;
   attn_status_t st;
   if ((st = map_2d(&ma, A, M, K, gb300::GEMM_BK, gb300::GEMM_BM_CTA)) != ATTN_OK) return st;
   if ((st = map_2d(&mb, Bm, K, N, 64, gb300::GEMM_BK)) != ATTN_OK) return st;
-  if ((st = map_2d(&mc, C, M, N, 64, 32)) != ATTN_OK) return st;  // epilogue store boxes
   if (!ds->gemm_attr.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
     // re-checked under the lock, as in launch_attn
@@ -340,6 +339,7 @@ attn_status_t run_gemm(DeviceState* ds, const void* A, const void* Bm, void* C, 
   p.n_tiles = N / gb300::GEMM_BN;
   p.k_blocks = K / gb300::GEMM_BK;
   p.C = static_cast<__nv_bfloat16*>(C);
+  p.c_v8 = aligned(C, 32) ? 1 : 0;  // rows are N * 2 bytes apart, a multiple of 512
   p.status = ds->status;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -360,7 +360,7 @@ attn_status_t run_gemm(DeviceState* ds, const void* A, const void* Bm, void* C, 
   const int pairs = p.n_list < ds->gemm_pairs ? p.n_list : ds->gemm_pairs;
   if (launch_kernel(gb300::gemm_bf16_kernel, static_cast<unsigned>(2 * pairs),
                     gb300::GEMM_THREADS, gb300::GemmLayout::SMEM_BYTES, stream, dependent, ma, mb,
-                    mc, p) != cudaSuccess)
+                    p) != cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;
 }

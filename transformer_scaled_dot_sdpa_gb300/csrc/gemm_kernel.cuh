@@ -20,7 +20,7 @@ constexpr int GEMM_BM_CTA = 128;
 constexpr int GEMM_BN = 256;        // columns of a tile: B split 128 / 128 over the pair
 constexpr int GEMM_BN_CTA = 128;
 constexpr int GEMM_BK = 64;
-constexpr int GEMM_STAGES = 6;
+constexpr int GEMM_STAGES = 7;
 constexpr int GEMM_THREADS = 192;
 constexpr uint32_t GEMM_TMEM_COLS = 512;
 enum : unsigned int { GEMM_STATUS_TIMEOUT = 1u };
@@ -30,11 +30,9 @@ struct GemmLayout {
   static constexpr int B_CHUNK = GEMM_BK * 64 * 2;             // 64 K-rows x 64 N = 8 KB
   static constexpr int B_BYTES = GEMM_BK * GEMM_BN_CTA * 2;    // 16 KB: this CTA's 128 columns
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;        // per CTA
-  static constexpr int C_BOX_BYTES = 32 * 64 * 2;              // 32 rows x 64 columns of C
   static constexpr int A_OFF = 0;
   static constexpr int B_OFF = GEMM_STAGES * A_BYTES;
-  static constexpr int C_OFF = B_OFF + GEMM_STAGES * B_BYTES;  // 2 staging boxes per epilogue warp
-  static constexpr int BAR_OFF = C_OFF + 4 * 2 * C_BOX_BYTES;
+  static constexpr int BAR_OFF = B_OFF + GEMM_STAGES * B_BYTES;
   static constexpr int B_FULL = 0;                       // used in the even CTA
   static constexpr int B_EMPTY = GEMM_STAGES;            // both CTAs
   static constexpr int B_ACC_FULL = 2 * GEMM_STAGES;     // both CTAs
@@ -56,6 +54,7 @@ struct GemmParams {
   // fit in one wave, so that wave takes half as long.
   int n_full, n_list;
   __nv_bfloat16* C;
+  int c_v8;  // C is 32-byte aligned: the epilogue writes 32-byte pieces
   unsigned int* status;
   unsigned long long wait_limit_ns;
 };
@@ -82,27 +81,27 @@ __device__ __forceinline__ int gemm_tile_coords(const GemmParams& p, int tile, i
 // One cluster = one pair of CTAs on a TPC; the pair computes 256 x 256 output
 // tiles, persistent over the tile list.  Per CTA of the pair:
 //   warp 0      TMA producer (one thread): its 128 rows of A and its 128
-//               columns of B into a 6-stage ring; the completion of both
+//               columns of B into a 7-stage ring; the completion of both
 //               CTAs' loads is counted on the even CTA's full-barrier
 //   warp 1      TMEM (both CTAs allocate the pair's 512 columns together);
 //               in the even CTA also the MMA issuer (whole warp, one elected
 //               lane issues tcgen05.mma.cta_group::2 with M = N = 256; its
 //               commits arrive on the barriers of both CTAs)
-//   warps 2-5   epilogue of this CTA's 128 rows: TMEM -> bf16 -> a 128B-
-//               swizzled staging box of 32 rows x 64 columns per warp (two,
-//               alternating) -> TMA tensor store; the four warps of each CTA
-//               release an accumulator with one arrival each on the even
-//               CTA's accumulator-empty barrier
-// Row-per-thread global stores here (32 scattered 16-byte pieces per warp
-// instruction) held up the TMA loads and the MMAs of the next tile; the TMA
-// store writes whole 128-byte lines.
+//   warps 2-5   epilogue of this CTA's 128 rows: TMEM -> bf16 -> global
+//               memory, each lane writing its row in whole 32-byte sectors;
+//               the four warps of each CTA release an accumulator with one
+//               arrival each on the even CTA's accumulator-empty barrier
+// The epilogue of one tile runs while the next tile's operands stream in.
+// Staging C in shared memory for TMA tensor stores made those stores compete
+// with the operand loads (the tensor pipe idled ~8% more on the QKV shape);
+// direct stores of whole sectors do not, and the freed 32 KB hold a seventh
+// stage, which hides more of the DRAM latency of A's first reads.
 // Per SM and 64-deep K block the tensor core reads 32 KB of operands from
 // shared memory for 2 x 128 x 256 x 64 FLOPs, two thirds of what a one-CTA
 // 128 x 256 tile needs.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   using L = GemmLayout;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -243,8 +242,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const int wq = warp & 3;  // TMEM lane quarter = rows 32 wq .. 32 wq + 31 of this CTA
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(&bars[L::B_ACC_EMPTY]), 0u);
-    uint8_t* stage = smem + L::C_OFF + wq * 2 * L::C_BOX_BYTES;
-    uint32_t tcount = 0, n_stores = 0;
+    uint32_t tcount = 0;
     bool ok = true;
     for (int tile = pair; tile < n_tiles_total; tile += n_pairs, ++tcount) {
       const uint32_t acc = tcount & 1u;
@@ -254,9 +252,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       tc_fence_after();
       int m0, n0;
       const int width = gemm_tile_coords(p, tile, m0, n0);
-      const int box_row = m0 + static_cast<int>(rank) * GEMM_BM_CTA + wq * 32;
-      // M is a multiple of 128: a box of 32 rows lies wholly inside or past M
-      const bool rows_in = box_row < p.M;
+      const int row0 = m0 + static_cast<int>(rank) * GEMM_BM_CTA + wq * 32;
+      // M is a multiple of 128: this warp's 32 rows lie wholly inside or past M
+      const bool rows_in = row0 < p.M;
 #pragma unroll 1
       for (int c = 0; c < width / 64; ++c) {
         uint32_t r0[32], r1[32];
@@ -265,38 +263,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         tmem_ld_wait(r0);
         reg_fence(r1);
         if (rows_in) {
-          uint8_t* box = stage + (n_stores & 1u) * L::C_BOX_BYTES;
-          // the store issued two boxes ago has finished reading this buffer
-          if (lane == 0) bulk_wait_group_read<1>();
-          __syncwarp();
-          // row `lane` of the box: 8 pieces of 16 bytes, piece j at position
-          // j ^ (row % 8) (the 128-byte swizzle of the tensor map)
-          const uint32_t row_addr = smem_u32(box) + static_cast<uint32_t>(lane) * 128u;
+          // row `lane` of C, columns n0 + 64 c .. + 63
+          __nv_bfloat16* crow = p.C + static_cast<size_t>(row0 + lane) * p.N + n0 + 64 * c;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t* q = (j < 4) ? &r0[8 * j] : &r1[8 * (j - 4)];
-            st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
-                         pack_bf16x2(__uint_as_float(q[0]), __uint_as_float(q[1])),
-                         pack_bf16x2(__uint_as_float(q[2]), __uint_as_float(q[3])),
-                         pack_bf16x2(__uint_as_float(q[4]), __uint_as_float(q[5])),
-                         pack_bf16x2(__uint_as_float(q[6]), __uint_as_float(q[7])));
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t* f = (i < 2) ? &r0[16 * i] : &r1[16 * (i - 2)];
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              w[k] = pack_bf16x2(__uint_as_float(f[2 * k]), __uint_as_float(f[2 * k + 1]));
+            if (p.c_v8) {
+              st_global_v8(crow + 16 * i, w);
+            } else {
+              st_global_v4(crow + 16 * i, w[0], w[1], w[2], w[3]);
+              st_global_v4(crow + 16 * i + 8, w[4], w[5], w[6], w[7]);
+            }
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmC, box, n0 + 64 * c, box_row);
-            bulk_commit_group();
-          }
-          ++n_stores;
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty0 + acc * 8u);
     }
-    // the stores have read their boxes and written C before the CTA leaves
-    if (lane == 0) bulk_wait_group<0>();
-    __syncwarp();
   }
 
   // Neither CTA leaves (or frees TMEM) while the other may still signal it.

@@ -221,31 +221,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// 2-D tiled TMA store of a box from this CTA's shared memory; completion is
-// tracked per thread with bulk groups
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0,
-                                             int c1) {
-  GB300_CHECK(c0 >= 0 && c1 >= 0 && tma_inner_coord_ok(c0, 2), CHECK_TMA_COORD);
-  GB300_CHECK(swizzled_tile_ok(smem_u32(src)), CHECK_SMEM_ALIGN);
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(c0), "r"(c1)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// at most N of this thread's bulk groups still reading their shared memory
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// at most N of this thread's bulk groups not yet complete
-template <int N>
-__device__ __forceinline__ void bulk_wait_group() {
-  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
 // generic-proxy writes to shared memory become visible to the async proxy
 // (TMA) of this CTA
 __device__ __forceinline__ void fence_proxy_async_smem() {
