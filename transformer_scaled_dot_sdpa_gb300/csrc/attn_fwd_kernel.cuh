@@ -559,10 +559,16 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
       ++s_cnt;
       tc_fence_after();
       uint32_t ra[32], rb[32], rc[32], rd[32];
-      tmem_ld_32x32b_x32(s_tmem + 0u, ra);
-      tmem_ld_32x32b_x32(s_tmem + 32u, rb);
-      tmem_ld_32x32b_x32(s_tmem + 64u, rc);
-      tmem_ld_32x32b_x32(s_tmem + 96u, rd);
+      // d = 128: one load of the 128 columns (+0.5-1.5%); d = 64: four of 32
+      // (one load was equal to 4% slower there)
+      if constexpr (D == 128) {
+        tmem_ld_32x32b_x128(s_tmem, ra, rb, rc, rd);
+      } else {
+        tmem_ld_32x32b_x32(s_tmem + 0u, ra);
+        tmem_ld_32x32b_x32(s_tmem + 32u, rb);
+        tmem_ld_32x32b_x32(s_tmem + 64u, rc);
+        tmem_ld_32x32b_x32(s_tmem + 96u, rd);
+      }
       tmem_ld_wait(ra);
       reg_fence(rb);
       reg_fence(rc);
@@ -632,11 +638,10 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
       const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-mb, -mb);
       uint64_t lf_a = 0ull, lf_b = 0ull;
       float lb_a = 0.f, lb_b = 0.f, lb_c = 0.f, lb_d = 0.f;
+      // exponentials of the pairs [i0, i1) of one half (64 keys) of the tile
+      auto exps = [&](int half, int i0, int i1, uint32_t* pk) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
+        for (int i = i0; i < i1; i += 2) {
           float a0, a1, a2, a3;
           f2_unpack(f2_fma(f2_pack(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]), c2, nm2), a0,
                     a1);
@@ -655,13 +660,28 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
             lb_d = add_bf16hi_f32(lb_d, pk[i + 1]);
           }
         }
-        tmem_st_32x32b_x32(p_tmem + 32u * half, pk);
-        // each half goes to the MMA issuer as soon as it is in TMEM: the
-        // tensor core multiplies it into V while the other half is computed
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bars[L::B_P_FULL + 2 * t + half]);
-      }
+      };
+      // Half 0 of P is stored, then exponentials of half 1 run while that
+      // store completes; only then is half 0 handed to the MMA issuer, which
+      // multiplies it into V while the rest of half 1 is computed.  Waiting
+      // for the store right after it cost a store latency per half.  At
+      // d = 128 half 0 goes after 32 of half 1's 64 exponentials; at d = 64,
+      // where P.V is short, both halves go together at the end (measured:
+      // d = 64 +2-3%, d = 128 +0.2-0.6% over the per-half wait).
+      constexpr int P_SPLIT = (D == 64) ? 32 : 16;  // pairs of half 1 before half 0 goes
+      uint32_t pk0[32], pk1[32];
+      exps(0, 0, 32, pk0);
+      tmem_st_32x32b_x32(p_tmem, pk0);
+      exps(1, 0, P_SPLIT, pk1);
+      tmem_st_wait();
+      reg_fence(pk0);  // the store has read pk0 before its registers are reused
+      tc_fence_before();
+      mbar_arrive(&bars[L::B_P_FULL + 2 * t]);
+      exps(1, P_SPLIT, 32, pk1);
+      tmem_st_32x32b_x32(p_tmem + 32u, pk1);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars[L::B_P_FULL + 2 * t + 1]);
       {
         float x0, x1;
         f2_unpack(f2_add(lf_a, lf_b), x0, x1);
