@@ -542,12 +542,29 @@ class LayerRun:
         # each stage's kernel timed alone on the same shapes (for the roofline)
         N, dm, dk = w.B * w.L, w.d_model, w.d_k
         qkv = torch.empty((N, 3 * dm), dtype=torch.bfloat16, device=dev)
-        cat = torch.empty((N, dm), dtype=torch.bfloat16, device=dev)
+        # the W_O input: unit-normal values, as the concatenated heads are
+        cat = torch.empty((N, dm), dtype=torch.bfloat16, device=dev).normal_()
         x2 = self.x.view(N, dm)
-        ms_qkv = time_calls(lambda: g.gemm_bf16(x2, self.wqkv, out=qkv, stream=stream), steps,
-                            stream, dev, flush)
-        ms_wo = time_calls(lambda: g.gemm_bf16(cat, self.wo, out=self.y.view(N, dm),
-                                               stream=stream), steps, stream, dev, flush)
+        y2 = self.y.view(N, dm)
+        # each projection through this library and through torch.matmul
+        # (cuBLAS, for comparison only), timed the same way in alternating
+        # blocks of calls, so that both see the same clocks and power
+        gemms = {"qkv_gemm": (x2, self.wqkv, qkv), "wo_gemm": (cat, self.wo, y2)}
+        ours = {k: 0.0 for k in gemms}
+        theirs = {k: 0.0 for k in gemms}
+        blocks = 5 if steps >= 5 else 1
+        per = max(1, steps // blocks)
+        with torch.cuda.stream(stream):
+            for a, b, c in gemms.values():
+                torch.matmul(a, b, out=c)
+            for _ in range(blocks):
+                for k, (a, b, c) in gemms.items():
+                    ours[k] += time_calls(lambda: g.gemm_bf16(a, b, out=c, stream=stream), per,
+                                          stream, dev, flush) / blocks
+                    theirs[k] += time_calls(lambda: torch.matmul(a, b, out=c), per, stream, dev,
+                                            flush) / blocks
+        ms_qkv, ms_wo = ours["qkv_gemm"], ours["wo_gemm"]
+        mm_qkv, mm_wo = theirs["qkv_gemm"], theirs["wo_gemm"]
         qh = torch.empty((w.B, w.H, w.L, dk), dtype=torch.bfloat16, device=dev).normal_()
         kh, vh = torch.empty_like(qh).normal_(), torch.empty_like(qh).normal_()
         oh = torch.empty_like(qh)
@@ -555,15 +572,6 @@ class LayerRun:
                                                out=oh, return_lse=False, stream=stream),
                             steps, stream, dev, flush)
         g.check_device_status(stream)
-        # the two projections through torch.matmul (cuBLAS), timed the same
-        # way, for comparison only
-        with torch.cuda.stream(stream):
-            torch.matmul(x2, self.wqkv, out=qkv)
-            torch.matmul(cat, self.wo, out=self.y.view(N, dm))
-            mm_qkv = time_calls(lambda: torch.matmul(x2, self.wqkv, out=qkv), steps, stream, dev,
-                                flush)
-            mm_wo = time_calls(lambda: torch.matmul(cat, self.wo, out=self.y.view(N, dm)), steps,
-                               stream, dev, flush)
         return {"ms": ms, "ms_max": max_over_ranks(ms, world), "flushed": flush is not None,
                 "clocks": clk, "stage_ms": {"qkv_gemm": ms_qkv, "attention": ms_att,
                                             "wo_gemm": ms_wo},
