@@ -665,9 +665,10 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
       // store completes; only then is half 0 handed to the MMA issuer, which
       // multiplies it into V while the rest of half 1 is computed.  Waiting
       // for the store right after it cost a store latency per half.  At
-      // d = 128 half 0 goes after 32 of half 1's 64 exponentials; at d = 64,
-      // where P.V is short, both halves go together at the end (measured:
-      // d = 64 +2-3%, d = 128 +0.2-0.6% over the per-half wait).
+      // d = 128 half 0 goes after 32 of half 1's 64 exponentials; at d = 64
+      // after all of them, just before half 1 is stored (measured: d = 64
+      // +2-3%, d = 128 +0.2-0.6% over the per-half wait; at d = 64, handing
+      // half 0 over only after half 1's store was 9-11% slower).
       constexpr int P_SPLIT = (D == 64) ? 32 : 16;  // pairs of half 1 before half 0 goes
       uint32_t pk0[32], pk1[32];
       exps(0, 0, 32, pk0);
