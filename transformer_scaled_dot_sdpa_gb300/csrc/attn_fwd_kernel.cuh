@@ -559,15 +559,14 @@ __device__ __forceinline__ void attn_softmax_role(const int t, const AttnParams&
       ++s_cnt;
       tc_fence_after();
       uint32_t ra[32], rb[32], rc[32], rd[32];
-      // d = 128: one load of the 128 columns (+0.5-1.5%); d = 64: four of 32
-      // (one load was equal to 4% slower there)
+      // d = 128: one load of the 128 columns (+0.5-1.5% over four of 32);
+      // d = 64: two of 64 (+1-1.3%; one of 128 was from 1% faster to 4%
+      // slower there)
       if constexpr (D == 128) {
         tmem_ld_32x32b_x128(s_tmem, ra, rb, rc, rd);
       } else {
-        tmem_ld_32x32b_x32(s_tmem + 0u, ra);
-        tmem_ld_32x32b_x32(s_tmem + 32u, rb);
-        tmem_ld_32x32b_x32(s_tmem + 64u, rc);
-        tmem_ld_32x32b_x32(s_tmem + 96u, rd);
+        tmem_ld_32x32b_x64(s_tmem + 0u, ra, rb);
+        tmem_ld_32x32b_x64(s_tmem + 64u, rc, rd);
       }
       tmem_ld_wait(ra);
       reg_fence(rb);
