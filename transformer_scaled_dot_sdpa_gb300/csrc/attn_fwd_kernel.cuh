@@ -333,7 +333,8 @@ __device__ __forceinline__ void attn_tma_role(const CUtensorMap* tmQ, const CUte
 //                           [wait P_t(j), keys 64-127]  O_t += P V_j (keys 64-127)
 //                           S_t(j+1) = Q_t K_{j+1}^T
 // The softmax hands P over in two halves, so the tensor core multiplies the
-// first 64 keys of P into V while the softmax still computes the second.
+// first 64 keys of P into V while the softmax still finishes the second (at
+// D = 128 the rest of its exponentials, at D = 64 its store to TMEM).
 // S_t(j+1) overwrites the TMEM columns that hold P_t(j).  Both MMAs
 // come from the same thread in that order, and the tensor core executes one
 // thread's MMAs in issue order, so P_t(j) has been read before S_t(j+1)
